@@ -1,0 +1,206 @@
+/*
+ * boost_block.h -- C ABI of the GB300 (sm_103a) low-rank bottleneck block.
+ *
+ * The operation is the CoLA-style bottleneck of "BOOST: BOttleneck-Optimized
+ * Scalable Training Framework for Low-Rank Large Language Models"
+ * (arXiv 2512.12131; technical summary on gist.science, §2.1-§2.2):
+ *
+ *     s      = (mean_j x[t,j]^2 + eps)^-1/2              (RMSNorm statistics)
+ *     z      = s * (x @ (gamma (.) A))                  (grouped down-projection,
+ *                                                        1/rms deferred to the GEMM)
+ *     a      = act(z)                                   (bottleneck nonlinearity)
+ *     y[i]   = a[:, i*r:(i+1)*r] @ B[i],  i < k         (batched up-projection)
+ *
+ * forward and backward, bf16 storage with fp32 accumulation.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensors are dense, row-major, bf16 (passed as raw 16-bit storage,
+ *   `const void*` / `void*`) unless stated; fp32 tensors are `float*`.
+ *   Device pointers must be device memory of the current device; host
+ *   pointers are marked "host".
+ * - The caller owns every buffer. The library allocates nothing, keeps no
+ *   state between calls, and writes only to the outputs and the workspace.
+ * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *   stream). Every argument is validated on the host before anything is
+ *   enqueued; a call that returns an error has enqueued nothing.
+ * - Device pointers must be 16-byte aligned. d, k*r, n (and r) must be
+ *   multiples of 8 so that every row starts on a 16-byte boundary.
+ * - Errors found on the device (a bounded wait that ran out) are recorded in
+ *   the workspace's error word and reported by boost_block_check().
+ * - Thread safety: calls on different workspaces may run concurrently.
+ */
+#ifndef BOOST_BLOCK_H
+#define BOOST_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BOOST_OK = 0,
+    BOOST_ERR_INVALID_ARG = 1,       /* NULL where a tensor is required, bad enum, negative size */
+    BOOST_ERR_UNSUPPORTED_SHAPE = 2, /* d % S != 0, dims not multiples of 8, sizes over limits */
+    BOOST_ERR_ALIGNMENT = 3,         /* a pointer is not 16-byte aligned */
+    BOOST_ERR_WORKSPACE = 4,         /* workspace NULL, misaligned or smaller than required */
+    BOOST_ERR_CUDA = 5,              /* a CUDA runtime call failed (no device, launch failure) */
+    BOOST_ERR_TIMEOUT = 6,           /* a kernel's bounded wait ran out (device-side) */
+    BOOST_ERR_DEVICE_CHECK = 7       /* a kernel recorded an internal consistency failure */
+} boost_status;
+
+typedef enum { BOOST_ACT_IDENTITY = 0, BOOST_ACT_SILU = 1 } boost_act;
+
+/*
+ * Shape of one bottleneck block.
+ *   T        tokens (rows of x), >= 0
+ *   d        input width (the hidden size of the pages' [b,s,d] activations)
+ *   r        bottleneck rank per group (the pages' low-rank dimension r)
+ *   k        number of grouped projections sharing x (3 for Q/K/V, 2 for gate/up)
+ *   n        output width of each up-projection
+ *   S        number of column shards of d whose sum-of-squares partials are
+ *            computed separately and combined once (Online-RMSNorm, §2.2);
+ *            1 <= S and d % S == 0. Only used when has_norm != 0.
+ *   eps      RMSNorm epsilon, added to the mean square inside the sqrt
+ *   act      boost_act: SiLU (CoLA) or identity (SVD-style bottleneck)
+ *   has_norm 1: the block starts with RMSNorm (gamma, rstd, dgamma used);
+ *            0: no norm (s == 1, gamma/rstd/dgamma must be NULL)
+ */
+typedef struct {
+    int64_t T, d, r, k, n;
+    int32_t S;
+    float eps;
+    int32_t act;
+    int32_t has_norm;
+} boost_block_desc;
+
+/* Size in bytes of the workspace boost_block_fwd and boost_block_bwd need for
+ * `desc` (the larger of the two; 0 for an invalid desc). The workspace is
+ * caller-owned device memory, 256-byte aligned, reusable across calls with the
+ * same or a smaller desc; its first 256 bytes hold the error word. */
+size_t boost_block_workspace_bytes(const boost_block_desc* desc);
+
+/* Clear the workspace's error word (asynchronous, on `stream`). */
+boost_status boost_block_ws_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Forward of one block (technical summary §2.2: Online-RMSNorm, linear-layer
+ * grouping).
+ *   x      [T, d]          input activations
+ *   gamma  [d]             RMSNorm weight (NULL iff has_norm == 0)
+ *   A      [d, k*r]        concatenated down-projection weights; group i is
+ *                          columns [i*r, (i+1)*r)
+ *   B      [k, r, n]       up-projection weights, one [r, n] matrix per group
+ *   y      [k, T, n]       out: y[i] = act(s * x @ (gamma (.) A))[:, group i] @ B[i]
+ *   rstd   [T] fp32        out, optional (NULL to skip): the row scale s,
+ *                          which boost_block_bwd may take back instead of
+ *                          recomputing it. Must be NULL when has_norm == 0.
+ *   ws     workspace of boost_block_workspace_bytes(desc) bytes or more
+ * Steps enqueued: sharded row statistics with one combine; gamma folded into
+ * A (bf16); one tensor-core GEMM over all k groups with s and act applied in
+ * its epilogue (the normalised x is never written); one batched tensor-core
+ * GEMM for the k up-projections.
+ */
+boost_status boost_block_fwd(const boost_block_desc* desc,
+                             const void* x, const void* gamma, const void* A, const void* B,
+                             void* y, float* rstd,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward of one block with recompute (technical summary §2.2,
+ * communication-free low-rank activation checkpointing: only x is kept; the
+ * r-wide activation is regenerated inside the block).
+ *   x, gamma, A, B   as in boost_block_fwd
+ *   rstd   [T] fp32  s from the forward, or NULL to recompute it from x
+ *   dy     [k, T, n] upstream gradient of y
+ *   dx     [T, d]    out: gradient of x (through the RMSNorm Jacobian)
+ *   dgamma [d]       out: gradient of gamma (NULL iff has_norm == 0)
+ *   dA     [d, k*r]  out: gradient of A
+ *   dB     [k, r, n] out: gradient of B
+ * Steps enqueued: (stats if rstd is NULL), fold, one tensor-core kernel with
+ * two TMEM accumulators per tile (z recomputed from x, and dy_i @ B_i^T)
+ * whose epilogue writes a, dzs = s * act'(z) * (dy B^T) and per-row partials
+ * of sum_m dz*z; dB = a^T dy and G = x^T dzs (split-K when too few tiles);
+ * dA = gamma (.) G and dgamma_j = sum_m A_jm G_jm; dx = dzs @ A'^T minus the
+ * RMSNorm row term (s^2/d) (sum_m dz z) x, applied in the GEMM epilogue.
+ */
+boost_status boost_block_bwd(const boost_block_desc* desc,
+                             const void* x, const void* gamma, const void* A, const void* B,
+                             const float* rstd, const void* dy,
+                             void* dx, void* dgamma, void* dA, void* dB,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Online-RMSNorm statistics alone (technical summary §2.2): per-shard sums of
+ * squares and their single combine.
+ *   x     [T, d]
+ *   ssq   [S, T] fp32 out: ssq[s, t] = sum over columns [s*d/S, (s+1)*d/S) of x[t,j]^2
+ *   rstd  [T] fp32   out: (sum_s ssq[s,t] / d + eps)^-1/2, shards summed in index order
+ * desc->has_norm must be 1.
+ */
+boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x,
+                                 float* ssq, float* rstd, void* stream);
+
+/*
+ * Exact bookkeeping of the shard and group partition (host only, no CUDA).
+ *   shard_off       host [S+1]: shard s covers columns [shard_off[s], shard_off[s+1]) of d
+ *   group_col_off   host [k+1]: group i covers columns [off[i], off[i+1]) of A
+ *   exchange_elems  host [1]: values in the one exchange that carries the
+ *                   bottleneck partials plus the statistics, T*(k*r+1)
+ *                   (technical summary §2.1: payload [b,s,r] instead of [b,s,d])
+ * Any output pointer may be NULL.
+ */
+boost_status boost_block_layout(const boost_block_desc* desc, int64_t* shard_off,
+                                int64_t* group_col_off, int64_t* exchange_elems);
+
+/* Byte offsets, inside a workspace for `desc`, of the tensors the block keeps there
+ * between its kernels (host only): a [T, k*r] bf16 (the bottleneck activation,
+ * written by the forward and again by the backward's recompute), dzs [T, k*r]
+ * bf16, the folded weight A' [d, k*r] bf16 and rstd [T] fp32 (used when the
+ * caller passes no rstd). Any output pointer may be NULL. For tests and
+ * inspection; the contents are only meaningful after the producing call. */
+boost_status boost_block_ws_layout(const boost_block_desc* desc, size_t* off_a, size_t* off_dzs,
+                                   size_t* off_Ap, size_t* off_rstd);
+
+/* Synchronise `stream`, then read and clear the workspace's error word.
+ * Returns BOOST_OK, BOOST_ERR_TIMEOUT / BOOST_ERR_DEVICE_CHECK recorded by a
+ * kernel, or BOOST_ERR_CUDA if the stream reports an error. */
+boost_status boost_block_check(void* ws, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* boost_status_string(boost_status status);
+
+/*
+ * SwiGLU between the gate/up bottleneck and the down bottleneck of the LLaMA
+ * MLP shape the pages evaluate (technical summary §4):
+ *   h = silu(gate) * up, elementwise over [T, n].
+ */
+boost_status boost_swiglu_fwd(int64_t T, int64_t n, const void* gate, const void* up,
+                              void* h, void* stream);
+
+/* Backward of boost_swiglu_fwd: dgate = dh * up * silu'(gate), dup = dh * silu(gate).
+ * dgate and dup may be the two halves of one [2, T, n] buffer. */
+boost_status boost_swiglu_bwd(int64_t T, int64_t n, const void* gate, const void* up,
+                              const void* dh, void* dgate, void* dup, void* stream);
+
+/* Residual add out = a + b over `count` bf16 elements (count % 8 == 0);
+ * out may alias a or b. */
+boost_status boost_add(int64_t count, const void* a, const void* b, void* out, void* stream);
+
+/*
+ * Self-test of the bounded wait every kernel uses (failure detection without a
+ * GPU fault): launches one tiny kernel that waits on an mbarrier nothing
+ * arrives on, with a wait limit of `limit_us` microseconds (1..10^6). The
+ * kernel gives up, records BOOST_ERR_TIMEOUT in the workspace's error word and
+ * returns; boost_block_check() then reports it and the context stays usable.
+ */
+boost_status boost_debug_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
+                                      void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BOOST_BLOCK_H */

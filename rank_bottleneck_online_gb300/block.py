@@ -1,0 +1,175 @@
+"""Workloads composed from the C-ABI calls: one block, the LLaMA MLP, the full
+layer without its attention core, and the SVD-style pair.
+
+Each workload owns its device tensors (weights, saved activations, gradients
+and one workspace) so that a training step is a fixed sequence of library
+calls on one stream with no allocation inside it. Every arithmetic step runs
+in the library's CUDA kernels; Python only sequences the calls.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+from .inputs import CONFIGS
+
+
+def _dev(t, device):
+    return None if t is None else t.to(device=device, non_blocking=False).contiguous()
+
+
+class Block:
+    """One bottleneck block: y = B_i . act(s * x @ (gamma A))_i, forward and backward."""
+
+    def __init__(self, T, d, r, k, n, *, S=1, eps=1e-5, act="silu", has_norm=True,
+                 weights=None, device="cuda", ws=None):
+        self.desc = B.make_desc(T, d, r, k, n, S=S, eps=eps, act=act, has_norm=has_norm)
+        self.device = torch.device(device)
+        w = weights or {}
+        self.gamma = _dev(w.get("gamma"), self.device) if has_norm else None
+        self.A = _dev(w.get("A"), self.device)
+        self.B = _dev(w.get("B"), self.device)
+        need = B.workspace_bytes(self.desc)
+        self.ws = ws.ensure(need) if ws is not None else B.Workspace(need, self.device)
+        bf = torch.bfloat16
+        self.y = torch.empty(k, T, n, dtype=bf, device=self.device)
+        self.rstd = torch.empty(T, dtype=torch.float32, device=self.device) if has_norm else None
+        self.dx = torch.empty(T, d, dtype=bf, device=self.device)
+        self.dA = torch.empty(d, k * r, dtype=bf, device=self.device)
+        self.dB = torch.empty(k, r, n, dtype=bf, device=self.device)
+        self.dgamma = torch.empty(d, dtype=bf, device=self.device) if has_norm else None
+
+    def forward(self, x, stream=None):
+        return B.block_fwd(self.desc, x, self.gamma, self.A, self.B, self.ws, y=self.y,
+                           rstd=self.rstd, stream=stream)
+
+    def backward(self, x, dy, stream=None, reuse_rstd=True):
+        return B.block_bwd(self.desc, x, self.gamma, self.A, self.B, dy, self.ws,
+                           rstd=self.rstd if reuse_rstd else None, dx=self.dx,
+                           dgamma=self.dgamma, dA=self.dA, dB=self.dB, stream=stream)
+
+
+class MLP:
+    """LLaMA MLP of two bottlenecks: gate/up (normed, k=2) -> SwiGLU -> down (k=1)."""
+
+    def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, act="silu", weights=None,
+                 device="cuda", ws=None):
+        w = weights or {}
+        self.T, self.d, self.ffn = T, d, ffn
+        self.gu = Block(T, d, r, 2, ffn, S=S, eps=eps, act=act, has_norm=True,
+                        weights={"gamma": w.get("gamma"), "A": w.get("A1"), "B": w.get("B1")},
+                        device=device, ws=ws)
+        self.dn = Block(T, ffn, r, 1, d, S=1, eps=eps, act=act, has_norm=False,
+                        weights={"A": w.get("A2"), "B": w.get("B2")}, device=device,
+                        ws=self.gu.ws)
+        self.gu.ws = self.dn.ws       # one workspace sized for both blocks
+        dev = self.gu.device
+        self.h = torch.empty(T, ffn, dtype=torch.bfloat16, device=dev)
+        self.dy1 = torch.empty(2, T, ffn, dtype=torch.bfloat16, device=dev)
+
+    @property
+    def out(self):
+        return self.dn.y[0]
+
+    def forward(self, x, stream=None):
+        y1 = self.gu.forward(x, stream)
+        B.swiglu_fwd(y1[0], y1[1], self.h, stream=stream)
+        return self.dn.forward(self.h, stream)[0]
+
+    def backward(self, x, dout, stream=None):
+        dh = self.dn.backward(self.h, dout.view(1, self.T, self.d), stream)[0]
+        B.swiglu_bwd(self.gu.y[0], self.gu.y[1], dh, self.dy1[0], self.dy1[1], stream=stream)
+        return self.gu.backward(x, self.dy1, stream)
+
+    def grads(self):
+        return {"dx": self.gu.dx, "dgamma": self.gu.dgamma, "dA1": self.gu.dA, "dB1": self.gu.dB,
+                "dA2": self.dn.dA, "dB2": self.dn.dB}
+
+
+class Layer:
+    """QKV (normed, k=3) -> O (k=1) on V -> residual -> MLP -> residual."""
+
+    def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, act="silu", weights=None, device="cuda"):
+        p = weights or {}
+        self.T, self.d = T, d
+        self.qkv = Block(T, d, r, 3, d, S=S, eps=eps, act=act, has_norm=True,
+                         weights={"gamma": p.get("gamma1"), "A": p.get("A_qkv"),
+                                  "B": p.get("B_qkv")}, device=device)
+        ws = self.qkv.ws
+        self.o = Block(T, d, r, 1, d, S=1, eps=eps, act=act, has_norm=False,
+                       weights={"A": p.get("A_o"), "B": p.get("B_o")}, device=device, ws=ws)
+        self.mlp = MLP(T, d, r, ffn, S=S, eps=eps, act=act,
+                       weights={"gamma": p.get("gamma2"), "A1": p.get("A_gu"), "B1": p.get("B_gu"),
+                                "A2": p.get("A_dn"), "B2": p.get("B_dn")}, device=device, ws=ws)
+        ws = self.mlp.gu.ws
+        for blk in (self.qkv, self.o):
+            blk.ws = ws
+        dev = self.qkv.device
+        bf = torch.bfloat16
+        self.x1 = torch.empty(T, d, dtype=bf, device=dev)
+        self.out = torch.empty(T, d, dtype=bf, device=dev)
+        self.dx1 = torch.empty(T, d, dtype=bf, device=dev)
+        self.dqkv = torch.empty(3, T, d, dtype=bf, device=dev)
+        self.dx = torch.empty(T, d, dtype=bf, device=dev)
+
+    def forward(self, x, stream=None):
+        qkv = self.qkv.forward(x, stream)
+        o = self.o.forward(qkv[2], stream)[0]
+        B.add(x, o, self.x1, stream=stream)
+        m = self.mlp.forward(self.x1, stream)
+        return B.add(self.x1, m, self.out, stream=stream)
+
+    def backward(self, x, dout, dq, dk, stream=None):
+        dxm = self.mlp.backward(self.x1, dout, stream)[0]
+        B.add(dout, dxm, self.dx1, stream=stream)
+        self.dqkv[0].copy_(dq)
+        self.dqkv[1].copy_(dk)
+        self.o.backward(self.qkv.y[2], self.dx1.view(1, self.T, self.d), stream)
+        self.dqkv[2].copy_(self.o.dx)
+        dxq = self.qkv.backward(x, self.dqkv, stream)[0]
+        return B.add(self.dx1, dxq, self.dx, stream=stream)
+
+
+class SVDPair:
+    """Two normed SVD-style bottlenecks (identity act) on one x: QKV and gate/up."""
+
+    def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, weights=None, device="cuda"):
+        p = weights or {}
+        self.qkv = Block(T, d, r, 3, d, S=S, eps=eps, act="identity", has_norm=True,
+                         weights={"gamma": p.get("gamma_qkv"), "A": p.get("A_qkv"),
+                                  "B": p.get("B_qkv")}, device=device)
+        self.gu = Block(T, d, r, 2, ffn, S=S, eps=eps, act="identity", has_norm=True,
+                        weights={"gamma": p.get("gamma_gu"), "A": p.get("A_gu"),
+                                 "B": p.get("B_gu")}, device=device, ws=self.qkv.ws)
+        self.qkv.ws = self.gu.ws
+        self.dx = torch.empty(T, d, dtype=torch.bfloat16, device=self.qkv.device)
+
+    def forward(self, x, stream=None):
+        return self.qkv.forward(x, stream), self.gu.forward(x, stream)
+
+    def backward(self, x, dy_qkv, dy_gu, stream=None):
+        self.qkv.backward(x, dy_qkv, stream)
+        self.gu.backward(x, dy_gu, stream)
+        return B.add(self.qkv.dx, self.gu.dx, self.dx, stream=stream)
+
+
+def build_workload(name, tensors, device="cuda", T=None):
+    """Instantiate a named workload with its (CPU) input tensors moved to ``device``."""
+    c = dict(CONFIGS[name])
+    if T is not None:
+        c["T"] = T
+    eps = 1e-5
+    if c["kind"] == "block":
+        return Block(c["T"], c["d"], c["r"], c["k"], c["n"], S=c["S"], eps=eps, act=c["act"],
+                     weights=tensors, device=device)
+    if c["kind"] == "mlp":
+        return MLP(c["T"], c["d"], c["r"], c["ffn"], S=c["S"], eps=eps, act=c["act"],
+                   weights=tensors, device=device)
+    if c["kind"] == "layer":
+        return Layer(c["T"], c["d"], c["r"], c["ffn"], S=c["S"], eps=eps, act=c["act"],
+                     weights=tensors["p"], device=device)
+    if c["kind"] == "svd_pair":
+        return SVDPair(c["T"], c["d"], c["r"], c["ffn"], S=c["S"], eps=eps,
+                       weights=tensors["p"], device=device)
+    raise KeyError(name)

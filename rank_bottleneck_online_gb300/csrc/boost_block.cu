@@ -1,0 +1,614 @@
+// boost_block.cu -- C ABI of the bottleneck block: argument validation, workspace
+// layout, launch plans, TMA tensor maps, and the forward/backward launch sequences.
+//
+// Operation: the CoLA-style low-rank bottleneck of "BOOST: BOttleneck-Optimized
+// Scalable Training Framework for Low-Rank Large Language Models" (technical
+// summary §2.1-§2.2): Online-RMSNorm statistics with deferred normalisation,
+// grouped down-projection over concatenated weights, batched up-projection, and a
+// backward that recomputes the bottleneck activation inside the block.
+#include "boost_block.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace boost_gb300 {
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
+                                  cudaStream_t stream);
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
+                                  cudaStream_t stream);
+
+cudaError_t launch_gemm(int bn, int mode, const GemmParams& p, int num_sms, cudaStream_t stream) {
+  if (mode == EPI_ACT || mode == EPI_BF16) return launch_gemm_fwd_modes(bn, mode, p, num_sms, stream);
+  return launch_gemm_bwd_modes(bn, mode, p, num_sms, stream);
+}
+}  // namespace boost_gb300
+
+using namespace boost_gb300;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int64_t kMaxDim = (1ll << 31) - 1;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// --------------------------------------------------------------- devices
+int current_num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 148;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* e = std::getenv("BOOST_WAIT_LIMIT_MS");
+    double ms = e ? std::atof(e) : 2000.0;
+    if (!(ms > 0.0)) ms = 2000.0;
+    return static_cast<uint64_t>(ms * 1e6);
+  }();
+  return v;
+}
+
+// ----------------------------------------------------------- tensor maps
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// 3-D bf16 view: dims (d0 contiguous, d1, d2), byte strides of d1 and d2, box b0 x b1 x b2,
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A row-major [rows, cols] bf16 matrix (rows < 2^31), viewed 3-D as (cols, rows, 1).
+bool map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
+            uint32_t box_rows) {
+  return make_map(m, base, cols, rows, 1, cols * 2, rows * cols * 2, box_cols, box_rows, 1);
+}
+
+OperandView kmajor_2d() { return OperandView{1, 0, 2, 0}; }   // (k, mn, -)
+OperandView mnmajor_2d() { return OperandView{0, 1, 2, 1}; }  // (mn, k, -)
+
+// ------------------------------------------------------------------ plan
+struct Plan {
+  int64_t T, d, r, k, n, kr;
+  int bn_down;               // K2 / K4 tile width (grouped tiling over k groups of r)
+  int tiles_per_group;
+  int n_tiles_down;
+  int bn_up, bn_dx;
+  int bn_wB, splits_B, kbps_B;
+  int bn_wA, splits_A, kbps_A;
+  size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_part, total;
+};
+
+void choose_splits(int64_t tiles, int64_t nkb, int sms, int& splits, int& kbps) {
+  splits = 1;
+  kbps = static_cast<int>(nkb);
+  double best = 1e300;
+  for (int s = 1; s <= 8; ++s) {
+    if (s > 1 && nkb / s < 4) break;
+    const int64_t per = cdiv(nkb, s);
+    const int64_t s_eff = cdiv(nkb, per);
+    const int64_t waves = cdiv(tiles * s_eff, sms);
+    const double cost = static_cast<double>(waves * per) * (s_eff > 1 ? 1.03 : 1.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      splits = static_cast<int>(s_eff);
+      kbps = static_cast<int>(per);
+    }
+  }
+}
+
+Plan make_plan(const boost_block_desc& D, int sms) {
+  Plan P{};
+  P.T = D.T; P.d = D.d; P.r = D.r; P.k = D.k; P.n = D.n; P.kr = D.k * D.r;
+  P.bn_down = (D.r % 128 == 0) ? 128 : 64;
+  P.tiles_per_group = static_cast<int>(cdiv(D.r, P.bn_down));
+  P.n_tiles_down = static_cast<int>(P.k * P.tiles_per_group);
+  P.bn_up = (D.n >= 256) ? 256 : (D.n > 64 ? 128 : 64);
+  P.bn_dx = (D.d >= 256) ? 256 : (D.d > 64 ? 128 : 64);
+  const int64_t m_tiles_T = cdiv(std::max<int64_t>(D.T, 1), kBM);
+  const int64_t nkb_T = cdiv(std::max<int64_t>(D.T, 1), kBK);
+  P.bn_wB = (D.n >= 256) ? 256 : (D.n > 64 ? 128 : 64);
+  const int64_t tiles_B = D.k * cdiv(D.r, kBM) * cdiv(D.n, P.bn_wB);
+  choose_splits(tiles_B, nkb_T, sms, P.splits_B, P.kbps_B);
+  P.bn_wA = (P.kr >= 256) ? 256 : (P.kr > 64 ? 128 : 64);
+  const int64_t tiles_A = cdiv(D.d, kBM) * cdiv(P.kr, P.bn_wA);
+  choose_splits(tiles_A, nkb_T, sms, P.splits_A, P.kbps_A);
+  (void)m_tiles_T;
+
+  size_t off = align_up(sizeof(DeviceError));
+  P.off_rstd = off; off = align_up(off + sizeof(float) * D.T);
+  P.off_ssq = off;  off = align_up(off + sizeof(float) * D.T * std::max(D.S, 1));
+  P.off_Ap = off;   off = align_up(off + 2ull * D.d * P.kr);
+  P.off_a = off;    off = align_up(off + 2ull * D.T * P.kr);
+  P.off_dzs = off;  off = align_up(off + 2ull * D.T * P.kr);
+  P.off_q = off;    off = align_up(off + sizeof(float) * P.n_tiles_down * D.T);
+  P.off_dg = off;   off = align_up(off + sizeof(float) * cdiv(P.kr, P.bn_wA) * D.d);
+  const size_t partB = P.splits_B > 1 ? sizeof(float) * P.splits_B * D.k * D.r * D.n : 0;
+  const size_t partA = P.splits_A > 1 ? sizeof(float) * P.splits_A * D.d * P.kr : 0;
+  P.off_part = off; off = align_up(off + std::max(partA, partB));
+  P.total = off;
+  return P;
+}
+
+boost_status validate_desc(const boost_block_desc* D) {
+  if (D == nullptr) return BOOST_ERR_INVALID_ARG;
+  if (D->T < 0 || D->d < 1 || D->r < 1 || D->k < 1 || D->n < 1) return BOOST_ERR_INVALID_ARG;
+  if (D->act != BOOST_ACT_IDENTITY && D->act != BOOST_ACT_SILU) return BOOST_ERR_INVALID_ARG;
+  if (D->has_norm != 0 && D->has_norm != 1) return BOOST_ERR_INVALID_ARG;
+  if (D->has_norm) {
+    if (D->S < 1) return BOOST_ERR_INVALID_ARG;
+    if (!(D->eps >= 0.0f) || !std::isfinite(D->eps)) return BOOST_ERR_INVALID_ARG;
+    if (D->d % D->S != 0) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (D->d % 8 || D->r % 8 || D->n % 8) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  const int64_t kr = D->k * D->r;
+  if (D->T > kMaxDim || D->d > kMaxDim || kr > kMaxDim || D->n > kMaxDim || D->k > 65535)
+    return BOOST_ERR_UNSUPPORTED_SHAPE;
+  // every row of every tensor and the flattened [k*T] / [k*r] extents fit 32-bit coordinates
+  if (D->k * D->T > kMaxDim || D->k * D->r > kMaxDim) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  return BOOST_OK;
+}
+
+boost_status check_ptrs(std::initializer_list<const void*> required,
+                        std::initializer_list<const void*> optional) {
+  for (const void* p : required) {
+    if (p == nullptr) return BOOST_ERR_INVALID_ARG;
+    if (!aligned16(p)) return BOOST_ERR_ALIGNMENT;
+  }
+  for (const void* p : optional)
+    if (p != nullptr && !aligned16(p)) return BOOST_ERR_ALIGNMENT;
+  return BOOST_OK;
+}
+
+boost_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return BOOST_ERR_WORKSPACE;
+  if (ws_bytes < need) return BOOST_ERR_WORKSPACE;
+  return BOOST_OK;
+}
+
+template <typename T>
+T* ws_at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+boost_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BOOST_OK;
+  return BOOST_ERR_CUDA;
+}
+
+GemmParams base_params(const Plan& P, DeviceError* err) {
+  GemmParams g;
+  std::memset(&g, 0, sizeof(g));
+  g.splits = 1;
+  g.batch = 1;
+  g.num_seg = 1;
+  g.err = err;
+  g.wait_limit_ns = wait_limit_ns();
+  (void)P;
+  return g;
+}
+
+// Down-projection GEMM parameters shared by the forward (K2) and the recompute (K4):
+// M = T, N = k*r tiled per group, K = d; A operand x (K-major), B operand A' (MN-major).
+bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap) {
+  if (!map_2d(&g.tmA[0], x, P.T, P.d, 64, kBM)) return false;
+  if (!map_2d(&g.tmB[0], Ap, P.d, P.kr, 64, 64)) return false;
+  g.seg[0].a = kmajor_2d();
+  g.seg[0].b = mnmajor_2d();
+  g.seg[0].num_kb = static_cast<int32_t>(cdiv(P.d, kBK));
+  g.M = static_cast<int32_t>(P.T);
+  g.N = static_cast<int32_t>(P.kr);
+  g.m_tiles = static_cast<int32_t>(cdiv(P.T, kBM));
+  g.n_tiles = P.n_tiles_down;
+  g.group_n = static_cast<int32_t>(P.r);
+  g.group_tiles = P.tiles_per_group;
+  g.m_inner = 0;
+  return true;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char* boost_status_string(boost_status s) {
+  switch (s) {
+    case BOOST_OK: return "ok";
+    case BOOST_ERR_INVALID_ARG: return "invalid argument";
+    case BOOST_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case BOOST_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case BOOST_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case BOOST_ERR_CUDA: return "CUDA runtime error";
+    case BOOST_ERR_TIMEOUT: return "device wait timed out";
+    case BOOST_ERR_DEVICE_CHECK: return "device consistency check failed";
+  }
+  return "unknown status";
+}
+
+size_t boost_block_workspace_bytes(const boost_block_desc* desc) {
+  if (validate_desc(desc) != BOOST_OK) return 0;
+  return make_plan(*desc, current_num_sms()).total;
+}
+
+boost_status boost_block_ws_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || ws_bytes < sizeof(DeviceError) ||
+      (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+    return BOOST_ERR_WORKSPACE;
+  return cuda_status(
+      cudaMemsetAsync(ws, 0, sizeof(DeviceError), static_cast<cudaStream_t>(stream)));
+}
+
+boost_status boost_block_layout(const boost_block_desc* desc, int64_t* shard_off,
+                                int64_t* group_col_off, int64_t* exchange_elems) {
+  boost_status st = validate_desc(desc);
+  if (st != BOOST_OK) return st;
+  const int32_t S = desc->has_norm ? desc->S : 1;
+  if (desc->d % S != 0) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  if (shard_off)
+    for (int32_t s = 0; s <= S; ++s) shard_off[s] = s * (desc->d / S);
+  if (group_col_off)
+    for (int64_t i = 0; i <= desc->k; ++i) group_col_off[i] = i * desc->r;
+  if (exchange_elems) *exchange_elems = desc->T * (desc->k * desc->r + 1);
+  return BOOST_OK;
+}
+
+boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x, float* ssq,
+                                 float* rstd, void* stream) {
+  boost_status st = validate_desc(desc);
+  if (st != BOOST_OK) return st;
+  if (!desc->has_norm) return BOOST_ERR_INVALID_ARG;
+  if (desc->T == 0) return BOOST_OK;
+  st = check_ptrs({x, rstd}, {ssq});
+  if (st != BOOST_OK) return st;
+  return cuda_status(launch_rmsnorm_stats(x, desc->T, desc->d, desc->S, desc->eps, ssq, rstd,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const void* gamma,
+                             const void* A, const void* B, void* y, float* rstd, void* ws,
+                             size_t ws_bytes, void* stream) {
+  boost_status st = validate_desc(desc);
+  if (st != BOOST_OK) return st;
+  const boost_block_desc& D = *desc;
+  if (!D.has_norm && (gamma != nullptr || rstd != nullptr)) return BOOST_ERR_INVALID_ARG;
+  // With no tokens the [T, ...] tensors are empty and may be NULL.
+  st = D.T == 0 ? check_ptrs({A, B}, {gamma, rstd, x, y}) : check_ptrs({x, A, B, y}, {gamma, rstd});
+  if (st != BOOST_OK) return st;
+  if (D.has_norm && gamma == nullptr) return BOOST_ERR_INVALID_ARG;
+  const int sms = current_num_sms();
+  const Plan P = make_plan(D, sms);
+  st = check_ws(ws, ws_bytes, P.total);
+  if (st != BOOST_OK) return st;
+  if (D.T == 0) return BOOST_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceError* err = ws_at<DeviceError>(ws, 0);
+
+  const void* Ap = A;
+  float* rs = nullptr;
+  if (D.has_norm) {
+    rs = rstd ? rstd : ws_at<float>(ws, P.off_rstd);
+    cudaError_t e = launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq),
+                                         rs, s);
+    if (e != cudaSuccess) return BOOST_ERR_CUDA;
+    e = launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s);
+    if (e != cudaSuccess) return BOOST_ERR_CUDA;
+    Ap = ws_at<void>(ws, P.off_Ap);
+  }
+  void* a = ws_at<void>(ws, P.off_a);
+
+  // K2: a = act(s * (x @ A')) over all k groups in one GEMM.
+  GemmParams g = base_params(P, err);
+  if (!down_segment(g, P, x, Ap)) return BOOST_ERR_CUDA;
+  g.act = D.act;
+  g.rstd = rs;
+  g.out = a;
+  g.ldo = P.kr;
+  cudaError_t e = launch_gemm(P.bn_down, EPI_ACT, g, sms, s);
+  if (e != cudaSuccess) return BOOST_ERR_CUDA;
+
+  // K3: y[i] = a[:, group i] @ B[i], batched over the k groups.
+  GemmParams u = base_params(P, err);
+  if (!make_map(&u.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, kBM)) return BOOST_ERR_CUDA;
+  if (!make_map(&u.tmB[0], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, 64, 1))
+    return BOOST_ERR_CUDA;
+  u.seg[0].a = OperandView{2, 0, 1, 0};   // a as (r, k, T): K-major, batch = group
+  u.seg[0].b = OperandView{0, 1, 2, 1};   // B as (n, r, k): MN-major
+  u.seg[0].num_kb = static_cast<int32_t>(cdiv(P.r, kBK));
+  u.M = static_cast<int32_t>(P.T);
+  u.N = static_cast<int32_t>(P.n);
+  u.batch = static_cast<int32_t>(P.k);
+  u.m_tiles = static_cast<int32_t>(cdiv(P.T, kBM));
+  u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.bn_up));
+  u.m_inner = 0;
+  u.out = y;
+  u.ldo = P.n;
+  u.out_bstride = P.T * P.n;
+  e = launch_gemm(P.bn_up, EPI_BF16, u, sms, s);
+  return cuda_status(e);
+}
+
+boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const void* gamma,
+                             const void* A, const void* B, const float* rstd, const void* dy,
+                             void* dx, void* dgamma, void* dA, void* dB, void* ws,
+                             size_t ws_bytes, void* stream) {
+  boost_status st = validate_desc(desc);
+  if (st != BOOST_OK) return st;
+  const boost_block_desc& D = *desc;
+  if (!D.has_norm && (gamma != nullptr || rstd != nullptr || dgamma != nullptr))
+    return BOOST_ERR_INVALID_ARG;
+  st = D.T == 0 ? check_ptrs({A, B, dA, dB}, {gamma, rstd, dgamma, x, dy, dx})
+                : check_ptrs({x, A, B, dy, dx, dA, dB}, {gamma, rstd, dgamma});
+  if (st != BOOST_OK) return st;
+  if (D.has_norm && (gamma == nullptr || dgamma == nullptr)) return BOOST_ERR_INVALID_ARG;
+  const int sms = current_num_sms();
+  const Plan P = make_plan(D, sms);
+  st = check_ws(ws, ws_bytes, P.total);
+  if (st != BOOST_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (D.T == 0) {  // no tokens: weight gradients are zero, dx is empty
+    cudaError_t e = cudaMemsetAsync(dA, 0, 2ull * D.d * P.kr, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, 2ull * D.k * D.r * D.n, s);
+    if (e == cudaSuccess && dgamma) e = cudaMemsetAsync(dgamma, 0, 2ull * D.d, s);
+    return cuda_status(e);
+  }
+  DeviceError* err = ws_at<DeviceError>(ws, 0);
+
+  const void* Ap = A;
+  const float* rs = nullptr;
+  if (D.has_norm) {
+    if (rstd == nullptr) {
+      float* r = ws_at<float>(ws, P.off_rstd);
+      if (launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq), r, s) !=
+          cudaSuccess)
+        return BOOST_ERR_CUDA;
+      rs = r;
+    } else {
+      rs = rstd;
+    }
+    if (launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s) != cudaSuccess)
+      return BOOST_ERR_CUDA;
+    Ap = ws_at<void>(ws, P.off_Ap);
+  }
+  void* a = ws_at<void>(ws, P.off_a);
+  void* dzs = ws_at<void>(ws, P.off_dzs);
+  float* qpart = ws_at<float>(ws, P.off_q);
+
+  // K4: per tile two accumulators, z (recomputed, K = d) and dy_i @ B_i^T (K = n).
+  GemmParams g = base_params(P, err);
+  if (!down_segment(g, P, x, Ap)) return BOOST_ERR_CUDA;
+  if (!make_map(&g.tmA[1], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, kBM, 1))
+    return BOOST_ERR_CUDA;
+  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, P.bn_down, 1))
+    return BOOST_ERR_CUDA;
+  g.num_seg = 2;
+  g.seg[1].a = OperandView{1, 0, 2, 0};   // dy as (n, T, k): K-major, batch = group
+  g.seg[1].b = OperandView{1, 0, 2, 0};   // B as (n, r, k): K-major rows of B_i
+  g.seg[1].num_kb = static_cast<int32_t>(cdiv(P.n, kBK));
+  g.seg[1].batch_from_n = 1;
+  g.seg[1].b_n_local = 1;
+  g.act = D.act;
+  g.rstd = rs;
+  g.out = a;
+  g.out2 = dzs;
+  g.ldo = P.kr;
+  g.qpart = D.has_norm ? qpart : nullptr;
+  cudaError_t e = launch_gemm(P.bn_down, EPI_DUAL, g, sms, s);
+  if (e != cudaSuccess) return BOOST_ERR_CUDA;
+
+  float* part = ws_at<float>(ws, P.off_part);
+
+  // K5: dB[i] = a[:, group i]^T @ dy[i]  (M = r, N = n, K = T).
+  {
+    GemmParams w = base_params(P, err);
+    if (!make_map(&w.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, 64)) return BOOST_ERR_CUDA;
+    if (!make_map(&w.tmB[0], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, 64, 1))
+      return BOOST_ERR_CUDA;
+    w.seg[0].a = OperandView{0, 2, 1, 1};  // a as (r, k, T): MN-major, K = T
+    w.seg[0].b = OperandView{0, 1, 2, 1};  // dy as (n, T, k): MN-major, K = T
+    w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.T, kBK));
+    w.M = static_cast<int32_t>(P.r);
+    w.N = static_cast<int32_t>(P.n);
+    w.batch = static_cast<int32_t>(P.k);
+    w.m_tiles = static_cast<int32_t>(cdiv(P.r, kBM));
+    w.n_tiles = static_cast<int32_t>(cdiv(P.n, P.bn_wB));
+    w.m_inner = 1;
+    w.ldo = P.n;
+    w.out_bstride = P.r * P.n;
+    if (P.splits_B > 1) {
+      w.splits = P.splits_B;
+      w.kb_per_split = P.kbps_B;
+      w.out = part;
+      w.out_sstride = P.k * P.r * P.n;
+      e = launch_gemm(P.bn_wB, EPI_F32, w, sms, s);
+      if (e == cudaSuccess) e = launch_splitk_sum_bf16(part, P.splits_B, P.k * P.r * P.n, dB, s);
+    } else {
+      w.out = dB;
+      e = launch_gemm(P.bn_wB, EPI_BF16, w, sms, s);
+    }
+    if (e != cudaSuccess) return BOOST_ERR_CUDA;
+  }
+
+  // K6: G = x^T @ dzs (M = d, N = k*r, K = T); dA = gamma (.) G, dgamma = rowsum(A (.) G).
+  {
+    GemmParams w = base_params(P, err);
+    if (!map_2d(&w.tmA[0], x, P.T, P.d, 64, 64)) return BOOST_ERR_CUDA;
+    if (!map_2d(&w.tmB[0], dzs, P.T, P.kr, 64, 64)) return BOOST_ERR_CUDA;
+    w.seg[0].a = mnmajor_2d();
+    w.seg[0].b = mnmajor_2d();
+    w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.T, kBK));
+    w.M = static_cast<int32_t>(P.d);
+    w.N = static_cast<int32_t>(P.kr);
+    w.m_tiles = static_cast<int32_t>(cdiv(P.d, kBM));
+    w.n_tiles = static_cast<int32_t>(cdiv(P.kr, P.bn_wA));
+    w.m_inner = 1;
+    w.ldo = P.kr;
+    if (P.splits_A > 1) {
+      w.splits = P.splits_A;
+      w.kb_per_split = P.kbps_A;
+      w.out = part;
+      w.out_sstride = P.d * P.kr;
+      e = launch_gemm(P.bn_wA, EPI_F32, w, sms, s);
+      if (e == cudaSuccess)
+        e = launch_splitk_finalize_dA(part, P.splits_A, P.d, P.kr, D.has_norm ? gamma : nullptr,
+                                      A, dA, D.has_norm ? dgamma : nullptr, s);
+    } else {
+      w.out = dA;
+      w.gamma = D.has_norm ? static_cast<const __nv_bfloat16*>(gamma) : nullptr;
+      w.wA = D.has_norm ? static_cast<const __nv_bfloat16*>(A) : nullptr;
+      w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
+      e = launch_gemm(P.bn_wA, EPI_DA, w, sms, s);
+      if (e == cudaSuccess && D.has_norm)
+        e = launch_dgamma_reduce(ws_at<float>(ws, P.off_dg), w.n_tiles, P.d, dgamma, s);
+    }
+    if (e != cudaSuccess) return BOOST_ERR_CUDA;
+  }
+
+  // K7: dx = dzs @ A'^T - (s^2 q / d) x  (M = T, N = d, K = k*r).
+  {
+    GemmParams w = base_params(P, err);
+    if (!map_2d(&w.tmA[0], dzs, P.T, P.kr, 64, kBM)) return BOOST_ERR_CUDA;
+    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.bn_dx)) return BOOST_ERR_CUDA;
+    w.seg[0].a = kmajor_2d();
+    w.seg[0].b = kmajor_2d();
+    w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.kr, kBK));
+    w.M = static_cast<int32_t>(P.T);
+    w.N = static_cast<int32_t>(P.d);
+    w.m_tiles = static_cast<int32_t>(cdiv(P.T, kBM));
+    w.n_tiles = static_cast<int32_t>(cdiv(P.d, P.bn_dx));
+    w.m_inner = 0;
+    w.out = dx;
+    w.ldo = P.d;
+    if (D.has_norm) {
+      w.rstd = rs;
+      w.qpart = qpart;
+      w.nq = P.n_tiles_down;
+      w.d_norm = static_cast<int32_t>(P.d);
+      w.xin = static_cast<const __nv_bfloat16*>(x);
+    }
+    e = launch_gemm(P.bn_dx, EPI_DX, w, sms, s);
+  }
+  return cuda_status(e);
+}
+
+boost_status boost_block_ws_layout(const boost_block_desc* desc, size_t* off_a, size_t* off_dzs,
+                                   size_t* off_Ap, size_t* off_rstd) {
+  boost_status st = validate_desc(desc);
+  if (st != BOOST_OK) return st;
+  const Plan P = make_plan(*desc, current_num_sms());
+  if (off_a) *off_a = P.off_a;
+  if (off_dzs) *off_dzs = P.off_dzs;
+  if (off_Ap) *off_Ap = P.off_Ap;
+  if (off_rstd) *off_rstd = P.off_rstd;
+  return BOOST_OK;
+}
+
+boost_status boost_block_check(void* ws, void* stream) {
+  if (ws == nullptr) return BOOST_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return BOOST_ERR_CUDA;
+  DeviceError h;
+  e = cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return BOOST_ERR_CUDA;
+  if (h.code != 0) {
+    DeviceError z{};
+    cudaMemcpy(ws, &z, sizeof(z), cudaMemcpyHostToDevice);
+    if (h.code == kErrTimeout) return BOOST_ERR_TIMEOUT;
+    return BOOST_ERR_DEVICE_CHECK;
+  }
+  return BOOST_OK;
+}
+
+boost_status boost_swiglu_fwd(int64_t T, int64_t n, const void* gate, const void* up, void* h,
+                              void* stream) {
+  if (T < 0 || n < 0) return BOOST_ERR_INVALID_ARG;
+  if (n % 8) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  if (T * n == 0) return BOOST_OK;
+  boost_status st = check_ptrs({gate, up, h}, {});
+  if (st != BOOST_OK) return st;
+  return cuda_status(launch_swiglu_fwd(gate, up, h, T * n, static_cast<cudaStream_t>(stream)));
+}
+
+boost_status boost_swiglu_bwd(int64_t T, int64_t n, const void* gate, const void* up,
+                              const void* dh, void* dgate, void* dup, void* stream) {
+  if (T < 0 || n < 0) return BOOST_ERR_INVALID_ARG;
+  if (n % 8) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  if (T * n == 0) return BOOST_OK;
+  boost_status st = check_ptrs({gate, up, dh, dgate, dup}, {});
+  if (st != BOOST_OK) return st;
+  return cuda_status(
+      launch_swiglu_bwd(gate, up, dh, dgate, dup, T * n, static_cast<cudaStream_t>(stream)));
+}
+
+boost_status boost_add(int64_t count, const void* a, const void* b, void* out, void* stream) {
+  if (count < 0) return BOOST_ERR_INVALID_ARG;
+  if (count % 8) return BOOST_ERR_UNSUPPORTED_SHAPE;
+  if (count == 0) return BOOST_OK;
+  boost_status st = check_ptrs({a, b, out}, {});
+  if (st != BOOST_OK) return st;
+  return cuda_status(launch_add(a, b, out, count, static_cast<cudaStream_t>(stream)));
+}
+
+boost_status boost_debug_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
+                                      void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return BOOST_ERR_INVALID_ARG;
+  boost_status st = check_ws(ws, ws_bytes, sizeof(DeviceError));
+  if (st != BOOST_OK) return st;
+  return cuda_status(launch_wait_timeout_probe(ws_at<DeviceError>(ws, 0),
+                                               static_cast<uint64_t>(limit_us) * 1000ull,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

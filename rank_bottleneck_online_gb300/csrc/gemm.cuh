@@ -1,0 +1,516 @@
+// gemm.cuh -- persistent, warp-specialised tcgen05 GEMM engine for sm_103a with the
+// bottleneck block's fused epilogues.
+//
+// One CTA per SM walks a static list of output tiles (128 x BN). Roles:
+//   warp 0, lane 0 : TMA producer; fills a ring of shared-memory stages
+//                    (A tile 128x64, B tile BNx64, bf16, 128-byte swizzle)
+//   warp 1         : allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
+//                    into a TMEM accumulator and commits stage/accumulator barriers
+//   warps 2..5     : epilogue; tcgen05.ld of the accumulator (one TMEM lane quarter
+//                    per warp, one output row per thread), fused math, global stores
+// Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
+// mainloop of tile i+1. Every mbarrier wait is bounded (ptx.cuh).
+//
+// Operands are described by "views" of 3-D tensor maps: which map dimension
+// carries the MN index, which the K index and which the batch index, and whether
+// the operand is K-major (K contiguous) or MN-major (MN contiguous). This lets one
+// kernel read x, a, dzs, dy and the weights in their natural row-major layouts,
+// including transposed uses (x^T, a^T, dy^T) without any transpose pass.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace boost_gb300 {
+
+constexpr int kBM = 128;           // rows per tile (TMEM lanes)
+constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
+constexpr int kNumThreads = 192;   // 6 warps
+constexpr int kEpiThreads = 128;   // warps 2..5
+
+enum EpiMode : int {
+  EPI_ACT = 0,     // out_bf16 = act(s_row * acc)               (down-projection fwd)
+  EPI_BF16 = 1,    // out_bf16 = acc                            (up-projection, dB)
+  EPI_F32 = 2,     // out_f32[split] = acc                      (split-K partials)
+  EPI_DUAL = 3,    // two accumulators: a, dzs, per-row q partials (recompute + dgrad)
+  EPI_DX = 4,      // out_bf16 = acc - (s^2 q / d) x            (dgrad x + RMSNorm bwd)
+  EPI_DA = 5,      // out_bf16 = gamma_row * acc, dgamma partials (wgrad of A)
+};
+
+struct OperandView {
+  int8_t mn_dim;    // tensor-map dimension carrying the M (or N) index
+  int8_t k_dim;     // dimension carrying K
+  int8_t b_dim;     // dimension carrying the batch / group index
+  int8_t mn_major;  // 1: MN contiguous (boxes 64 MN x 64 K); 0: K contiguous (box 64 K x rows)
+};
+
+struct Segment {
+  OperandView a, b;
+  int32_t num_kb;        // k-blocks of 64 over the whole K of this segment
+  int32_t batch_from_n;  // batch index = the tile's group instead of the tile's batch
+  int32_t b_n_local;     // B operand's MN coordinate is the column within the group
+  int32_t pad;
+};
+
+struct GemmParams {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  Segment seg[2];
+  int32_t num_seg;
+  int32_t M, N;               // output extent (per batch)
+  int32_t batch;              // batches in the tile list
+  int32_t m_tiles, n_tiles;
+  int32_t splits, kb_per_split;
+  int32_t m_inner;            // tile order: 1 = m fastest within (batch, split)
+  int32_t group_n;            // columns per group (grouped tiling)
+  int32_t group_tiles;        // >0: N tiled per group, this many tiles per group
+  int32_t act;                // 0 identity, 1 SiLU
+  int32_t d_norm;             // EPI_DX: full d of the RMSNorm mean
+  int32_t nq;                 // EPI_DX: number of q partial rows to sum
+  // epilogue tensors (elements, not bytes, for strides)
+  void* out;                  // bf16 or fp32 output
+  void* out2;                 // EPI_DUAL: dzs
+  int64_t ldo;                // leading dimension of out/out2
+  int64_t out_bstride;        // batch stride of out
+  int64_t out_sstride;        // split stride of out (EPI_F32)
+  const float* rstd;          // [M] row scale or nullptr (s == 1)
+  float* qpart;               // EPI_DUAL out / EPI_DX in: [n_tiles or nq][M]
+  float* dgpart;              // EPI_DA out: [n_tiles][M]
+  const __nv_bfloat16* xin;   // EPI_DX: x [M, N]
+  const __nv_bfloat16* gamma; // EPI_DA: gamma [M]
+  const __nv_bfloat16* wA;    // EPI_DA: A [M, N]
+  DeviceError* err;
+  uint64_t wait_limit_ns;
+};
+
+template <int BN, int MODE>
+struct GemmCfg {
+  static constexpr bool kDual = (MODE == EPI_DUAL);
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kAccCols = kDual ? 2 * BN : BN;            // columns per accumulator set
+  static constexpr int kAccStages = (2 * kAccCols <= 512) ? 2 : 1;
+  static constexpr int kTmemColsRaw = kAccStages * kAccCols;
+  static constexpr int kTmemCols = kTmemColsRaw <= 32 ? 32 : kTmemColsRaw <= 64 ? 64
+                                   : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAccStages + 1) + 16;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes;
+  static_assert(kTmemColsRaw <= 512, "TMEM overflow");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+};
+
+struct TileCoord {
+  int32_t batch, split, m0, n_blk;
+  int32_t n0, n_end;      // output columns [n0, n_end) of this tile
+  int32_t group, n_local; // grouped tiling: group index and column within the group
+};
+
+// Tiles are ordered (split, batch, outer, inner). With group_tiles > 0 the N
+// extent is tiled per group of group_n columns, so no tile straddles two groups.
+template <int BN>
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int32_t tile) {
+  const int32_t per = p.m_tiles * p.n_tiles;
+  const int32_t bs = tile / per;
+  const int32_t rem = tile - bs * per;
+  int32_t mb, nb;
+  if (p.m_inner) {
+    mb = rem % p.m_tiles;
+    nb = rem / p.m_tiles;
+  } else {
+    nb = rem % p.n_tiles;
+    mb = rem / p.n_tiles;
+  }
+  TileCoord c;
+  c.split = bs / p.batch;
+  c.batch = bs - c.split * p.batch;
+  c.m0 = mb * kBM;
+  c.n_blk = nb;
+  if (p.group_tiles > 0) {
+    c.group = nb / p.group_tiles;
+    c.n_local = (nb - c.group * p.group_tiles) * BN;
+    c.n0 = c.group * p.group_n + c.n_local;
+    c.n_end = min(c.n0 + BN, (c.group + 1) * p.group_n);
+  } else {
+    c.n0 = nb * BN;
+    c.n_end = min(c.n0 + BN, p.N);
+    c.group = 0;
+    c.n_local = c.n0;
+  }
+  return c;
+}
+
+__device__ __forceinline__ void kb_range(const GemmParams& p, int seg, int32_t split,
+                                         int32_t& kb0, int32_t& kb1) {
+  const int32_t nkb = p.seg[seg].num_kb;
+  if (p.splits <= 1) {
+    kb0 = 0;
+    kb1 = nkb;
+  } else {
+    kb0 = split * p.kb_per_split;
+    kb1 = min(nkb, kb0 + p.kb_per_split);
+  }
+}
+
+__device__ __forceinline__ void load_operand(const CUtensorMap* tm, const OperandView& v,
+                                             uint8_t* dst, uint64_t* bar, int32_t mn, int32_t k,
+                                             int32_t b, int rows) {
+  int32_t c[3] = {0, 0, 0};
+  c[v.k_dim] = k;
+  c[v.b_dim] = b;
+  if (v.mn_major) {
+    for (int j = 0; j < rows / 64; ++j) {
+      c[v.mn_dim] = mn + 64 * j;
+      tma_load_3d(dst + j * 8192, tm, bar, c[0], c[1], c[2]);
+    }
+  } else {
+    c[v.mn_dim] = mn;
+    tma_load_3d(dst, tm, bar, c[0], c[1], c[2]);
+  }
+}
+
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
+  // K-major: rows of 128 B (64 K), 8-row groups 1024 B apart; a K step of 16 is +32 B.
+  // MN-major: boxes of [64 K rows][64 MN], 8 KB apart along MN (LBO), 8-row K groups
+  // 1024 B apart (SBO); a K step of 16 is two groups, +2048 B.
+  return mn_major ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
+                  : smem_desc_sw128(base + kk * 32, 16, 1024);
+}
+
+__device__ __forceinline__ float act_fwd(float z, int act) {
+  if (act == 1) return z / (1.0f + __expf(-z));
+  return z;
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmParams p) {
+  using Cfg = GemmCfg<BN, MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + Cfg::kStages * Cfg::kABytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
+  uint64_t* empty_bar = full_bar + Cfg::kStages;
+  uint64_t* tfull_bar = empty_bar + Cfg::kStages;
+  uint64_t* tempty_bar = tfull_bar + Cfg::kAccStages;
+  uint64_t* done_bar = tempty_bar + Cfg::kAccStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t num_tiles = p.batch * p.splits * p.m_tiles * p.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < Cfg::kAccStages; ++s) {
+      mbar_init(&tfull_bar[s], 1);
+      mbar_init(&tempty_bar[s], kEpiThreads);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA[0]);
+    tma_prefetch_desc(&p.tmB[0]);
+    if (p.num_seg > 1) {
+      tma_prefetch_desc(&p.tmA[1]);
+      tma_prefetch_desc(&p.tmB[1]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed_parity[Cfg::kStages];
+      bool armed[Cfg::kStages];
+      for (int s = 0; s < Cfg::kStages; ++s) armed[s] = false, armed_parity[s] = 0;
+      bool ok = true;
+      for (int32_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const TileCoord tc = decode_tile<BN>(p, tile);
+        for (int sg = 0; sg < p.num_seg && ok; ++sg) {
+          const Segment& S = p.seg[sg];
+          int32_t b = tc.batch;
+          int32_t nb = tc.n0;
+          if (S.batch_from_n) b = tc.group;
+          if (S.b_n_local) nb = tc.n_local;
+          int32_t kb0, kb1;
+          kb_range(p, sg, tc.split, kb0, kb1);
+          for (int32_t kb = kb0; kb < kb1; ++kb) {
+            if (!bounded_wait(&empty_bar[stage], phase ^ 1u, p.err, 1, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], Cfg::kStageBytes);
+            armed[stage] = true;
+            armed_parity[stage] = phase;
+            load_operand(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage], tc.m0,
+                         kb * kBK, b, kBM);
+            load_operand(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage], nb,
+                         kb * kBK, b, BN);
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Drain: every copy this thread started has landed before the CTA exits.
+      for (int s = 0; s < Cfg::kStages; ++s) {
+        if (armed[s]) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full_bar[s], armed_parity[s])) {
+            if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+              record_error(p.err, kErrTimeout, 7);
+              break;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      uint32_t idesc[2];
+      for (int sg = 0; sg < 2; ++sg)
+        idesc[sg] = idesc_bf16_f32(kBM, BN, p.seg[sg].a.mn_major, p.seg[sg].b.mn_major);
+      for (int32_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const TileCoord tc = decode_tile<BN>(p, tile);
+        if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int sg = 0; sg < p.num_seg && ok; ++sg) {
+          const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols + sg * BN;
+          const int a_mn = p.seg[sg].a.mn_major, b_mn = p.seg[sg].b.mn_major;
+          int32_t kb0, kb1;
+          kb_range(p, sg, tc.split, kb0, kb1);
+          for (int32_t kb = kb0; kb < kb1; ++kb) {
+            if (!bounded_wait(&full_bar[stage], phase, p.err, 3, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes);
+            const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              tc_mma_bf16(d_tmem, operand_desc(a_base, a_mn, kk), operand_desc(b_base, b_mn, kk),
+                          idesc[sg], (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(&empty_bar[stage]);
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        tc_commit(&tfull_bar[acc]);
+        if (++acc == Cfg::kAccStages) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs issued by this thread are complete before TMEM is released.
+      tc_commit(done_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(done_bar, 0)) {
+        if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+          record_error(p.err, kErrTimeout, 8);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;                    // TMEM lane quarter of this warp
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int32_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const TileCoord tc = decode_tile<BN>(p, tile);
+      const int32_t n0 = tc.n0;
+      const int32_t n_end = tc.n_end;
+      if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
+      tc_fence_after();
+      const int32_t row = tc.m0 + row_in_tile;
+      const bool row_ok = row < p.M;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::kAccCols);
+      float s_row = 1.0f;
+      if constexpr (MODE == EPI_ACT || MODE == EPI_DUAL || MODE == EPI_DX) {
+        if (p.rstd != nullptr && row_ok) s_row = p.rstd[row];
+      }
+      float rowsum = 0.0f;
+      float coef = 0.0f;
+      if constexpr (MODE == EPI_DX) {
+        if (p.rstd != nullptr && row_ok) {
+          float qs = 0.0f;
+          for (int j = 0; j < p.nq; ++j) qs += p.qpart[static_cast<int64_t>(j) * p.M + row];
+          coef = s_row * s_row * qs / static_cast<float>(p.d_norm);
+        }
+      }
+      float g_row = 1.0f;
+      if constexpr (MODE == EPI_DA) {
+        if (p.gamma != nullptr && row_ok) g_row = __bfloat162float(p.gamma[row]);
+      }
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int32_t col0 = n0 + c * 32;
+        float v[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, v);
+        float w[32];
+        if constexpr (MODE == EPI_DUAL) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
+        tmem_ld_wait();
+        if constexpr (MODE == EPI_F32) {
+          if (row_ok) {
+            float* o = static_cast<float*>(p.out) + tc.split * p.out_sstride +
+                       tc.batch * p.out_bstride + static_cast<int64_t>(row) * p.ldo + col0;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              if (col0 + g * 4 < n_end)
+                *reinterpret_cast<float4*>(o + g * 4) =
+                    make_float4(v[g * 4], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+          }
+        } else {
+          uint32_t pk[16];
+          uint32_t pk2[16];
+          if constexpr (MODE == EPI_ACT) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act),
+                                  act_fwd(s_row * v[2 * i + 1], p.act));
+          } else if constexpr (MODE == EPI_BF16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          } else if constexpr (MODE == EPI_DUAL) {
+            float a_v[32], dzs_v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float z = s_row * v[i];
+              a_v[i] = act_fwd(z, p.act);   // same expression as EPI_ACT: bitwise recompute
+              float dz;
+              if (p.act == 1) {
+                const float sg = 1.0f / (1.0f + __expf(-z));
+                dz = w[i] * (sg * (1.0f + z * (1.0f - sg)));
+              } else {
+                dz = w[i];
+              }
+              if (col0 + i < n_end) rowsum += dz * z;
+              dzs_v[i] = s_row * dz;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              pk[i] = pack_bf16x2(a_v[2 * i], a_v[2 * i + 1]);
+              pk2[i] = pack_bf16x2(dzs_v[2 * i], dzs_v[2 * i + 1]);
+            }
+          } else if constexpr (MODE == EPI_DX) {
+            float xv[32];
+            if (row_ok && coef != 0.0f) {
+              const uint4* xp = reinterpret_cast<const uint4*>(
+                  p.xin + static_cast<int64_t>(row) * p.ldo + col0);
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (col0 + g * 8 < n_end) u = xp[g];
+                xv[g * 8 + 0] = bf16_lo(u.x); xv[g * 8 + 1] = bf16_hi(u.x);
+                xv[g * 8 + 2] = bf16_lo(u.y); xv[g * 8 + 3] = bf16_hi(u.y);
+                xv[g * 8 + 4] = bf16_lo(u.z); xv[g * 8 + 5] = bf16_hi(u.z);
+                xv[g * 8 + 6] = bf16_lo(u.w); xv[g * 8 + 7] = bf16_hi(u.w);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) xv[i] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(v[2 * i] - coef * xv[2 * i], v[2 * i + 1] - coef * xv[2 * i + 1]);
+          } else if constexpr (MODE == EPI_DA) {
+            if (row_ok && p.wA != nullptr) {
+              const uint4* ap = reinterpret_cast<const uint4*>(
+                  p.wA + static_cast<int64_t>(row) * p.ldo + col0);
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                if (col0 + g * 8 < n_end) {
+                  const uint4 u = ap[g];
+                  rowsum += bf16_lo(u.x) * v[g * 8 + 0] + bf16_hi(u.x) * v[g * 8 + 1] +
+                            bf16_lo(u.y) * v[g * 8 + 2] + bf16_hi(u.y) * v[g * 8 + 3] +
+                            bf16_lo(u.z) * v[g * 8 + 4] + bf16_hi(u.z) * v[g * 8 + 5] +
+                            bf16_lo(u.w) * v[g * 8 + 6] + bf16_hi(u.w) * v[g * 8 + 7];
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
+          }
+          if (row_ok) {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
+                               static_cast<int64_t>(row) * p.ldo + col0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              if (col0 + g * 8 < n_end)
+                *reinterpret_cast<uint4*>(o + g * 8) =
+                    make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            if constexpr (MODE == EPI_DUAL) {
+              __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
+                                  static_cast<int64_t>(row) * p.ldo + col0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (col0 + g * 8 < n_end)
+                  *reinterpret_cast<uint4*>(o2 + g * 8) =
+                      make_uint4(pk2[4 * g], pk2[4 * g + 1], pk2[4 * g + 2], pk2[4 * g + 3]);
+            }
+          }
+        }
+      }
+      if constexpr (MODE == EPI_DUAL) {
+        if (row_ok && p.qpart != nullptr)
+          p.qpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
+      }
+      if constexpr (MODE == EPI_DA) {
+        if (row_ok && p.dgpart != nullptr)
+          p.dgpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      if (++acc == Cfg::kAccStages) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace boost_gb300

@@ -1,0 +1,336 @@
+// kernels_simple.cu -- the block's HBM-bound CUDA-core kernels: Online-RMSNorm
+// statistics, the gamma fold, SwiGLU forward/backward, residual add, split-K
+// finalisation, the dgamma reduction and the bounded-wait self-test.
+// All bf16 traffic moves in 16-byte vectors (8 elements per thread access).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace boost_gb300 {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ float silu_grad_f(float z) {
+  const float g = 1.0f / (1.0f + __expf(-z));
+  return g * (1.0f + z * (1.0f - g));
+}
+
+// Online-RMSNorm statistics (BOOST technical summary §2.2): one warp per row.
+// ssq[s, t] is the fp32 sum of squares over shard s = columns [s*w, (s+1)*w);
+// the shards are then combined once, in index order, into rstd[t].
+__global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
+    float* __restrict__ ssq, float* __restrict__ rstd) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const __nv_bfloat16* xr = x + row * d;
+  const int64_t w = d / S;
+  float total = 0.0f;
+  for (int s = 0; s < S; ++s) {
+    const __nv_bfloat16* xs = xr + s * w;
+    float acc0 = 0.0f, acc1 = 0.0f;
+    if ((w & 7) == 0) {
+      const uint4* v = reinterpret_cast<const uint4*>(xs);
+      const int64_t nv = w >> 3;
+      int64_t i = lane;
+      for (; i + 32 < nv; i += 64) {
+        float f[8], g[8];
+        unpack8(__ldg(v + i), f);
+        unpack8(__ldg(v + i + 32), g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc0 = fmaf(f[e], f[e], acc0);
+          acc1 = fmaf(g[e], g[e], acc1);
+        }
+      }
+      for (; i < nv; i += 32) {
+        float f[8];
+        unpack8(__ldg(v + i), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc0 = fmaf(f[e], f[e], acc0);
+      }
+    } else {
+      for (int64_t i = lane; i < w; i += 32) {
+        const float f = __bfloat162float(xs[i]);
+        acc0 = fmaf(f, f, acc0);
+      }
+    }
+    const float part = warp_sum(acc0 + acc1);
+    if (lane == 0 && ssq != nullptr) ssq[static_cast<int64_t>(s) * T + row] = part;
+    total += part;  // the single combine, in shard order
+  }
+  if (lane == 0) rstd[row] = 1.0f / sqrtf(total / static_cast<float>(d) + eps);
+}
+
+// A'[j, m] = bf16(gamma_j * A[j, m]); the product of two bf16 values is exact in fp32.
+__global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
+    const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
+    __nv_bfloat16* __restrict__ Ap, int64_t d, int64_t kr) {
+  const int64_t nvec = d * kr / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t j = (i * 8) / kr;
+    const float g = __bfloat162float(gamma[j]);
+    float f[8];
+    unpack8(reinterpret_cast<const uint4*>(A)[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] *= g;
+    reinterpret_cast<uint4*>(Ap)[i] = pack8(f);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(
+    const uint4* __restrict__ g, const uint4* __restrict__ u, uint4* __restrict__ h, int64_t nvec) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float fg[8], fu[8], fh[8];
+    unpack8(g[i], fg);
+    unpack8(u[i], fu);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fh[e] = silu_f(fg[e]) * fu[e];
+    h[i] = pack8(fh);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(
+    const uint4* __restrict__ g, const uint4* __restrict__ u, const uint4* __restrict__ dh,
+    uint4* __restrict__ dg, uint4* __restrict__ du, int64_t nvec) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float fg[8], fu[8], fd[8], og[8], ou[8];
+    unpack8(g[i], fg);
+    unpack8(u[i], fu);
+    unpack8(dh[i], fd);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      og[e] = fd[e] * fu[e] * silu_grad_f(fg[e]);
+      ou[e] = fd[e] * silu_f(fg[e]);
+    }
+    dg[i] = pack8(og);
+    du[i] = pack8(ou);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) add_kernel(const uint4* a, const uint4* b, uint4* out,
+                                                       int64_t nvec) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float fa[8], fb[8];
+    unpack8(a[i], fa);
+    unpack8(b[i], fb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fa[e] += fb[e];
+    out[i] = pack8(fa);
+  }
+}
+
+// out = bf16(sum_s part[s]) over `count` elements, splits summed in index order.
+__global__ void __launch_bounds__(kThreads) splitk_sum_bf16_kernel(
+    const float4* __restrict__ part, int splits, int64_t count4, uint2* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < count4;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float4 acc = part[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = part[static_cast<int64_t>(s) * count4 + i];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    out[i] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+}
+
+// One warp per row j of G = sum_s part[s] ([d, kr]): dA = bf16(gamma_j * G[j, :]) and
+// dgamma_j = bf16(sum_m A[j, m] * G[j, m]). Without gamma: dA = bf16(G).
+__global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
+    const float* __restrict__ part, int splits, int64_t d, int64_t kr,
+    const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
+    __nv_bfloat16* __restrict__ dA, __nv_bfloat16* __restrict__ dgamma) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= d) return;
+  const float g = gamma != nullptr ? __bfloat162float(gamma[j]) : 1.0f;
+  const int64_t nv = kr / 8;
+  const int64_t plane = d * kr;
+  float acc = 0.0f;
+  for (int64_t i = lane; i < nv; i += 32) {
+    const int64_t off = j * kr + i * 8;
+    float G[8];
+    const float4 a0 = *reinterpret_cast<const float4*>(part + off);
+    const float4 a1 = *reinterpret_cast<const float4*>(part + off + 4);
+    G[0] = a0.x; G[1] = a0.y; G[2] = a0.z; G[3] = a0.w;
+    G[4] = a1.x; G[5] = a1.y; G[6] = a1.z; G[7] = a1.w;
+    for (int s = 1; s < splits; ++s) {
+      const float4 b0 = *reinterpret_cast<const float4*>(part + s * plane + off);
+      const float4 b1 = *reinterpret_cast<const float4*>(part + s * plane + off + 4);
+      G[0] += b0.x; G[1] += b0.y; G[2] += b0.z; G[3] += b0.w;
+      G[4] += b1.x; G[5] += b1.y; G[6] += b1.z; G[7] += b1.w;
+    }
+    float o[8];
+    if (gamma != nullptr) {
+      float a[8];
+      unpack8(*reinterpret_cast<const uint4*>(A + off), a);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc = fmaf(a[e], G[e], acc);
+        o[e] = g * G[e];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = G[e];
+    }
+    *reinterpret_cast<uint4*>(dA + off) = pack8(o);
+  }
+  if (dgamma != nullptr) {
+    acc = warp_sum(acc);
+    if (lane == 0) dgamma[j] = __float2bfloat16_rn(acc);
+  }
+}
+
+// dgamma_j = bf16(sum_t dgpart[t][j]), tiles summed in index order.
+__global__ void __launch_bounds__(kThreads) dgamma_reduce_kernel(
+    const float* __restrict__ dgpart, int ntiles, int64_t d, __nv_bfloat16* __restrict__ dgamma) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (j >= d) return;
+  float acc = 0.0f;
+  for (int t = 0; t < ntiles; ++t) acc += dgpart[static_cast<int64_t>(t) * d + j];
+  dgamma[j] = __float2bfloat16_rn(acc);
+}
+
+// Bounded-wait self-test: waits on an mbarrier that nothing arrives on. The wait
+// gives up after limit_ns, records the timeout and the kernel returns normally.
+__global__ void wait_timeout_probe_kernel(DeviceError* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    bool done = false;
+    while (!done) {
+      if (mbar_try_wait(&bar, 0)) break;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        record_error(err, kErrTimeout, 100);
+        done = true;
+      }
+    }
+    // Complete the barrier's phase so nothing is left pending at exit.
+    mbar_arrive(&bar);
+  }
+  __syncthreads();
+}
+
+int grid_for(int64_t work, int per_block) {
+  int64_t g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > 148 * 32) g = 148 * 32;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, float eps,
+                                 float* ssq, float* rstd, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int rows_per_block = kThreads / 32;
+  const int64_t grid = (T + rows_per_block - 1) / rows_per_block;
+  rmsnorm_stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_gamma(const void* gamma, const void* A, void* Ap, int64_t d, int64_t kr,
+                              cudaStream_t stream) {
+  if (d * kr == 0) return cudaSuccess;
+  fold_gamma_kernel<<<grid_for(d * kr / 8, kThreads), kThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(A),
+      static_cast<__nv_bfloat16*>(Ap), d, kr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_fwd(const void* g, const void* u, void* h, int64_t count,
+                              cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  swiglu_fwd_kernel<<<grid_for(count / 8, kThreads), kThreads, 0, stream>>>(
+      static_cast<const uint4*>(g), static_cast<const uint4*>(u), static_cast<uint4*>(h),
+      count / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd(const void* g, const void* u, const void* dh, void* dg, void* du,
+                              int64_t count, cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  swiglu_bwd_kernel<<<grid_for(count / 8, kThreads), kThreads, 0, stream>>>(
+      static_cast<const uint4*>(g), static_cast<const uint4*>(u), static_cast<const uint4*>(dh),
+      static_cast<uint4*>(dg), static_cast<uint4*>(du), count / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add(const void* a, const void* b, void* out, int64_t count,
+                       cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  add_kernel<<<grid_for(count / 8, kThreads), kThreads, 0, stream>>>(
+      static_cast<const uint4*>(a), static_cast<const uint4*>(b), static_cast<uint4*>(out),
+      count / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_sum_bf16(const float* part, int splits, int64_t count, void* out,
+                                   cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  splitk_sum_bf16_kernel<<<grid_for(count / 4, kThreads), kThreads, 0, stream>>>(
+      reinterpret_cast<const float4*>(part), splits, count / 4, static_cast<uint2*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_finalize_dA(const float* part, int splits, int64_t d, int64_t kr,
+                                      const void* gamma, const void* A, void* dA, void* dgamma,
+                                      cudaStream_t stream) {
+  if (d == 0) return cudaSuccess;
+  const int rows_per_block = kThreads / 32;
+  const int64_t grid = (d + rows_per_block - 1) / rows_per_block;
+  splitk_finalize_dA_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+      part, splits, d, kr, static_cast<const __nv_bfloat16*>(gamma),
+      static_cast<const __nv_bfloat16*>(A), static_cast<__nv_bfloat16*>(dA),
+      static_cast<__nv_bfloat16*>(dgamma));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgamma_reduce(const float* dgpart, int ntiles, int64_t d, void* dgamma,
+                                 cudaStream_t stream) {
+  if (d == 0) return cudaSuccess;
+  dgamma_reduce_kernel<<<static_cast<unsigned>((d + kThreads - 1) / kThreads), kThreads, 0,
+                         stream>>>(dgpart, ntiles, d, static_cast<__nv_bfloat16*>(dgamma));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_probe(DeviceError* err, uint64_t limit_ns, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace boost_gb300

@@ -1,0 +1,41 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI and
+the oracle on the same seeded inputs and compare with the stated tolerances.
+
+Tolerances (bf16 outputs and gradients, against the oracle's bf16 flow):
+max relative error 2e-2 and mean relative error 2e-3, with
+max_rel = max_i |g_i - o_i| / max(|o_i|, rms(o)) and mean_rel = sum|g-o| / sum|o|.
+"""
+
+import numpy as np
+import torch
+
+import oracle
+from rank_bottleneck_online_gb300 import inputs
+
+MAX_REL = 2e-2
+MEAN_REL = 2e-3
+
+
+def to_np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def assert_close(name, got, want, max_rel=MAX_REL, mean_rel=MEAN_REL):
+    g = to_np(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    w = np.asarray(want, np.float64)
+    assert g.shape == w.shape, (name, g.shape, w.shape)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    mx, mean = oracle.rel_errors(g, w)
+    assert mx <= max_rel and mean <= mean_rel, f"{name}: max_rel={mx:.3e} mean_rel={mean:.3e}"
+    return mx, mean
+
+
+def oracle_block(w, *, act, has_norm, S, eps=1e-5):
+    x = inputs.as_f64(w["x"])
+    g = inputs.as_f64(w["gamma"]) if has_norm else None
+    A = inputs.as_f64(w["A"])
+    Bw = inputs.as_f64(w["B"])
+    dy = inputs.as_f64(w["dy"])
+    y, c = oracle.block_fwd(x, g, A, Bw, act=act, has_norm=has_norm, eps=eps, S=S, flow="bf16")
+    gr = oracle.block_bwd(x, g, A, Bw, dy, act=act, has_norm=has_norm, eps=eps, S=S, flow="bf16")
+    return y, c, gr
