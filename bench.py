@@ -1,0 +1,432 @@
+"""Benchmark of the low-rank bottleneck hot path on GB300.
+
+One step = forward + backward of the LLaMA-2-7B-shaped CoLA MLP
+(T = 4 x 4096 tokens, d = 4096, r = 1024, ffn = 11008, S = 8 norm shards):
+gate/up bottleneck (Online-RMSNorm statistics, folded gamma, grouped
+down-projection with deferred 1/rms + SiLU, batched up-projection) -> SwiGLU ->
+down bottleneck, then the backward with low-rank recompute. Inputs are the
+seeded synthetic tensors of rank_bottleneck_online_gb300.inputs, resident in
+HBM before the timed region; every large tensor the step touches (x 134 MB, the
+gate/up activations 721 MB and their gradients) is larger than the 129 MB L2,
+so no L2 flush is inserted between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU (torchrun, one process per GPU) runs independent replicas (weak
+scaling); the only collectives are the timing barrier and the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bottleneck-block fwd+bwd TFLOP/s & tokens/s on 1 GB300; % of roofline"
+WORKLOAD = "llama2_7b_mlp"
+CPU_SAMPLE_T = 1024          # tokens of the CPU-baseline sample (full d, r, ffn)
+REF_SAMPLE_T = 256           # tokens per step of the reference arm
+
+
+def mlp_flops(T, d, r, ffn):
+    """Executed flops of one MLP step (recompute included) and model flops."""
+    blocks = [(d, 2 * r, ffn), (ffn, r, d)]          # (input width, k*r, n)
+    exe = sum(8 * T * din * kr + 6 * T * kr * n for din, kr, n in blocks)
+    model = sum(6 * T * din * kr + 6 * T * kr * n for din, kr, n in blocks)
+    return exe, model
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _cfg():
+    from rank_bottleneck_online_gb300.inputs import CONFIGS
+    return CONFIGS[WORKLOAD]
+
+
+# ------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index):
+        self.index = str(index)
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [[c.strip() for c in l.split(",")] for l in self.out.read().splitlines()
+                if l.strip()]
+        rows = [r for r in rows if len(r) >= 9]
+        if any(r[0] == self.index for r in rows):
+            rows = [r for r in rows if r[0] == self.index]
+        sm, smax, power, seen = [], [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(self.NAMES, r[5:9]):
+                if v.lower() == "active":
+                    seen.add(nm)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(seen), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- oracle
+
+def cpu_oracle_sample(T_sample, steps=1):
+    """Time the oracle (bf16 flow, fwd+bwd) on T_sample tokens of the workload.
+
+    Runs in a fresh subprocess with every BLAS/OpenMP pool sized to the cores
+    this process may use; returns seconds per step, tokens and thread count.
+    """
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(T_sample),
+           "--_oracle-steps", str(steps)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed: {r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["cores"] = cores
+    return res
+
+
+def _oracle_sample_main(T_sample, steps):
+    import oracle
+    from rank_bottleneck_online_gb300 import inputs
+
+    c = inputs.CONFIGS[WORKLOAD]
+    w = inputs.make_inputs(WORKLOAD, T=T_sample, seed=0)
+    f = {k: inputs.as_f64(v) for k, v in w.items()}
+    args = (f["x"], f["gamma"], f["A1"], f["B1"], f["A2"], f["B2"])
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.mlp_fwd(*args, S=c["S"], flow="bf16")
+        oracle.mlp_bwd(*args, f["dout"], S=c["S"], flow="bf16")
+        times.append(time.perf_counter() - t0)
+    print(json.dumps({"seconds": times, "tokens": T_sample}))
+
+
+def reference_arm(args, rank, world):
+    """The oracle, as it stands, on the host cores: rank 0 only."""
+    if rank != 0:
+        return 0
+    c = _cfg()
+    T_s = REF_SAMPLE_T
+    res = cpu_oracle_sample(T_s, steps=args.warmup + args.steps)
+    secs = res["seconds"][args.warmup:]
+    per = sum(secs) / len(secs)
+    value = T_s / per
+    exe, _ = mlp_flops(T_s, c["d"], c["r"], c["ffn"])
+    sample = (f"{T_s} of {c['T']} tokens of {WORKLOAD} per step (full d/r/ffn), oracle bf16 "
+              "flow fwd+bwd in numpy fp64")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens": c["T"], "d": c["d"], "r": c["r"],
+                       "ffn": c["ffn"], "S": c["S"], "l2": "inputs larger than L2"},
+            "tflops_per_s": exe / per / 1e12,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": res["cores"],
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- ours
+
+def csrc_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rank_bottleneck_online_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel, units):
+    """DRAM bytes of one launch of `kernel` from the committed ncu summary, scaled from
+    the captured case by units processed, or None when the kernel sources changed since
+    the counters were taken (the summary records a digest of csrc/)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = csrc_digest()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if line.startswith("#") or len(parts) < 4 or parts[0] != kernel:
+                continue
+            if parts[1] != digest:
+                return None
+            return float(parts[2]) * units / float(parts[3])
+    return None
+
+
+def ours_arm(args, rank, world, local_rank):
+    import torch
+
+    from rank_bottleneck_online_gb300 import binding as B
+    from rank_bottleneck_online_gb300 import build as build_mod
+    from rank_bottleneck_online_gb300 import inputs
+    from rank_bottleneck_online_gb300.block import MLP
+
+    build_mod.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    c = _cfg()
+    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
+    if args.tokens:
+        T = args.tokens
+    w = inputs.make_inputs(WORKLOAD, seed=0, T=T)
+    mlp = MLP(T, d, r, ffn, S=S, weights=w, device=dev)
+    x = w["x"].to(dev)
+    dout = w["dout"].to(dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mlp.forward(x)
+        mlp.backward(x, dout)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    B.check(mlp.gu.ws)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    B.profile_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    prof = B.profile_read()
+    B.profile_enable(False)
+    B.check(mlp.gu.ws)
+    ms_total = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    e2e_s = float("nan") if args.skip_aux else _e2e(args, mlp, w, x, dout, T, d, barrier,
+                                                    dist, dev)
+    bi = 2 * T * d * 2          # x and dout, bf16
+    bo = 2 * T * d * 2          # out and dx, bf16
+    if rank != 0:
+        return 0
+    return _report(args, world, prof, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn, S)
+
+
+def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
+    """Seconds for args.steps steps through the public API from pinned host buffers:
+    each step copies x and dout in, runs forward + backward, copies out and dx back."""
+    import torch
+
+    x_h = w["x"].pin_memory()
+    dout_h = w["dout"].pin_memory()
+    out_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+    dx_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        dout.copy_(dout_h, non_blocking=True)
+        mlp.forward(x)
+        mlp.backward(x, dout)
+        out_h.copy_(mlp.out, non_blocking=True)
+        dx_h.copy_(mlp.gu.dx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    return e2e_s
+
+
+def _report(args, world, prof, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn, S):
+    ms_step = ms_total / args.steps
+    tokens_per_s = world * T * args.steps / (ms_total / 1e3)
+    exe, model = mlp_flops(T, d, r, ffn)
+    tflops = world * exe * args.steps / (ms_total / 1e3) / 1e12
+    peaks = load_peaks()
+    # dominant kernel: the largest share of the timed region (event time per kernel)
+    name, (launches, kms, kfl, kby) = max(prof.items(), key=lambda kv: kv[1][1])
+    bound = "tensor" if kfl > 0 else "hbm"
+    if bound == "tensor":
+        achieved = kfl / (kms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+        per_launch_units = kfl / launches
+    else:
+        achieved = kby / (kms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+        per_launch_units = kby / launches
+    traffic = read_traffic(name, per_launch_units)
+    step_bytes = sum(v[3] for v in prof.values()) / args.steps
+    roof_ms = max(exe / (peaks["bf16_tflops"] * 1e12),
+                  step_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    gpu_launches = sum(v[0] for v in prof.values())
+
+    cpu = None
+    if world == 1 and not args.skip_aux:
+        try:
+            res = cpu_oracle_sample(CPU_SAMPLE_T, steps=1)
+            cpu = {"value": CPU_SAMPLE_T / res["seconds"][0], "unit": "tokens/s",
+                   "cores": res["cores"], "kind": "oracle",
+                   "sample": f"{CPU_SAMPLE_T} of {T} tokens of {WORKLOAD} (full d/r/ffn), "
+                             "oracle bf16 flow fwd+bwd in numpy fp64, one run"}
+        except Exception as ex:  # noqa: BLE001
+            cpu = {"value": None, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                   "kind": "oracle", "sample": f"failed: {ex}"[:200]}
+
+    total_ms = sum(u[1] for u in prof.values())
+    kernels = {k: {"launches": v[0], "ms": round(v[1], 4), "share": round(v[1] / total_ms, 4),
+                   "tflops": round(v[2] / (v[1] / 1e3) / 1e12, 1) if v[2] else None,
+                   "gbs": round(v[3] / (v[1] / 1e3) / 1e9, 1)}
+               for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])}
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": T, "d": d, "r": r, "ffn": ffn, "S": S,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "tflops_per_s": tflops,
+        "model_tflops_per_s": world * model * args.steps / (ms_total / 1e3) / 1e12,
+        "pct_of_roofline": 100.0 * roof_ms / ms_step,
+        "roofline_step": {"flops": exe, "bytes": step_bytes, "time_ms": roof_ms,
+                          "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
+                          "peaks": f"{peaks['source']} burst"},
+        "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                     "launches_per_step": launches / args.steps,
+                     "peak_kind": (f"{peaks['source']} sustained" if bound == "tensor"
+                                   else peaks["source"])},
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
+        "e2e": None if args.skip_aux else {
+            "value": world * T * args.steps / e2e_s, "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload on fewer tokens (profiling captures)")
+    ap.add_argument("--skip-aux", action="store_true",
+                    help="skip the end-to-end and CPU-baseline legs (profiling captures)")
+    ap.add_argument("--_oracle-sample", type=int, default=0, dest="oracle_sample")
+    ap.add_argument("--_oracle-steps", type=int, default=1, dest="oracle_steps")
+    args = ap.parse_args(argv)
+    if args.oracle_sample:
+        _oracle_sample_main(args.oracle_sample, args.oracle_steps)
+        return 0
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return ours_arm(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

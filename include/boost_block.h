@@ -199,6 +199,24 @@ boost_status boost_add(int64_t count, const void* a, const void* b, void* out, v
 boost_status boost_debug_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
                                       void* stream);
 
+/*
+ * Per-kernel timing of the library's own launches (measurement support; the
+ * pages define no such interface). While enabled, each launch is bracketed by
+ * two CUDA events on its stream and its algorithmic work (flops, bytes: every
+ * operand read once, every output written once) is accumulated per kernel.
+ *   boost_profile_enable(1) clears the counters and starts recording,
+ *   boost_profile_enable(0) stops; both first collect pending events.
+ *   boost_profile_kernel_count() is the number of kernel ids.
+ *   boost_profile_read(id, ...) synchronises the pending events and returns the
+ *   kernel's static name, launch count, summed event time in milliseconds and
+ *   summed algorithmic flops and bytes. Any output pointer may be NULL.
+ * Process-wide; intended for one measuring thread.
+ */
+boost_status boost_profile_enable(int on);
+int boost_profile_kernel_count(void);
+boost_status boost_profile_read(int id, const char** name, int64_t* launches, double* total_ms,
+                                double* total_flops, double* total_bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,8 @@ EXPORTS = (
     "boost_block_workspace_bytes", "boost_block_ws_init", "boost_block_fwd", "boost_block_bwd",
     "boost_rmsnorm_stats", "boost_block_layout", "boost_block_check", "boost_status_string",
     "boost_swiglu_fwd", "boost_swiglu_bwd", "boost_add", "boost_debug_wait_timeout",
-    "boost_block_ws_layout",
+    "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
+    "boost_profile_read",
 )
 
 
@@ -81,6 +82,11 @@ def lib():
     L.boost_debug_wait_timeout.argtypes = [vp, sz, u32, vp]
     szp = ctypes.POINTER(sz)
     L.boost_block_ws_layout.argtypes = [dp, szp, szp, szp, szp]
+    L.boost_profile_enable.argtypes = [ctypes.c_int]
+    L.boost_profile_kernel_count.argtypes = []
+    dbl = ctypes.POINTER(ctypes.c_double)
+    L.boost_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                     ctypes.POINTER(i64), dbl, dbl, dbl]
     for name in EXPORTS:
         if name != "boost_block_workspace_bytes" and name != "boost_status_string":
             getattr(L, name).restype = ctypes.c_int
@@ -273,6 +279,25 @@ def add(a, b, out=None, stream=None):
 def check(ws: Workspace, stream=None):
     """Synchronise and raise if a kernel recorded a device-side error."""
     _check(lib().boost_block_check(ws.ptr, _stream(stream)), "boost_block_check")
+
+
+def profile_enable(on: bool):
+    _check(lib().boost_profile_enable(1 if on else 0), "boost_profile_enable")
+
+
+def profile_read():
+    """{kernel name: (launches, total_ms, total_flops, total_bytes)} for kernels that ran."""
+    L = lib()
+    out = {}
+    for i in range(L.boost_profile_kernel_count()):
+        name = ctypes.c_char_p()
+        n = ctypes.c_int64(0)
+        ms, fl, by = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+        _check(L.boost_profile_read(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms),
+                                    ctypes.byref(fl), ctypes.byref(by)), "boost_profile_read")
+        if n.value:
+            out[name.value.decode()] = (n.value, ms.value, fl.value, by.value)
+    return out
 
 
 def debug_wait_timeout(ws: Workspace, limit_us: int, stream=None):

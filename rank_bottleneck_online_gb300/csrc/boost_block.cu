@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "profile.h"
 
 namespace boost_gb300 {
 cudaError_t launch_gemm_fwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
@@ -182,6 +183,9 @@ Plan make_plan(const boost_block_desc& D, int sms) {
   return P;
 }
 
+double stats_bytes(const Plan& P, int S) { return 2.0 * P.T * P.d + 4.0 * P.T * (S + 1); }
+double fold_bytes(const Plan& P) { return 4.0 * P.d * P.kr + 2.0 * P.d; }
+
 boost_status validate_desc(const boost_block_desc* D) {
   if (D == nullptr) return BOOST_ERR_INVALID_ARG;
   if (D->T < 0 || D->d < 1 || D->r < 1 || D->k < 1 || D->n < 1) return BOOST_ERR_INVALID_ARG;
@@ -312,8 +316,10 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x, fl
   if (desc->T == 0) return BOOST_OK;
   st = check_ptrs({x, rstd}, {ssq});
   if (st != BOOST_OK) return st;
-  return cuda_status(launch_rmsnorm_stats(x, desc->T, desc->d, desc->S, desc->eps, ssq, rstd,
-                                          static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Plan P = make_plan(*desc, current_num_sms());
+  ProfScope ps(s, K_STATS, 0.0, stats_bytes(P, desc->S));
+  return cuda_status(launch_rmsnorm_stats(x, desc->T, desc->d, desc->S, desc->eps, ssq, rstd, s));
 }
 
 boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const void* gamma,
@@ -339,10 +345,16 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   float* rs = nullptr;
   if (D.has_norm) {
     rs = rstd ? rstd : ws_at<float>(ws, P.off_rstd);
-    cudaError_t e = launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq),
-                                         rs, s);
+    cudaError_t e;
+    {
+      ProfScope ps(s, K_STATS, 0.0, stats_bytes(P, D.S));
+      e = launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq), rs, s);
+    }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
-    e = launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s);
+    {
+      ProfScope ps(s, K_FOLD, 0.0, fold_bytes(P));
+      e = launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s);
+    }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
     Ap = ws_at<void>(ws, P.off_Ap);
   }
@@ -355,7 +367,12 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   g.rstd = rs;
   g.out = a;
   g.ldo = P.kr;
-  cudaError_t e = launch_gemm(P.bn_down, EPI_ACT, g, sms, s);
+  cudaError_t e;
+  {
+    ProfScope ps(s, K_DOWN, 2.0 * P.T * P.d * P.kr,
+                 2.0 * (P.T * P.d + P.d * P.kr + P.T * P.kr) + 4.0 * P.T);
+    e = launch_gemm(P.bn_down, EPI_ACT, g, sms, s);
+  }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
   // K3: y[i] = a[:, group i] @ B[i], batched over the k groups.
@@ -375,7 +392,11 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   u.out = y;
   u.ldo = P.n;
   u.out_bstride = P.T * P.n;
-  e = launch_gemm(P.bn_up, EPI_BF16, u, sms, s);
+  {
+    ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
+                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
+    e = launch_gemm(P.bn_up, EPI_BF16, u, sms, s);
+  }
   return cuda_status(e);
 }
 
@@ -410,6 +431,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   if (D.has_norm) {
     if (rstd == nullptr) {
       float* r = ws_at<float>(ws, P.off_rstd);
+      ProfScope ps(s, K_STATS, 0.0, stats_bytes(P, D.S));
       if (launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq), r, s) !=
           cudaSuccess)
         return BOOST_ERR_CUDA;
@@ -417,8 +439,11 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     } else {
       rs = rstd;
     }
-    if (launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s) != cudaSuccess)
-      return BOOST_ERR_CUDA;
+    {
+      ProfScope ps(s, K_FOLD, 0.0, fold_bytes(P));
+      if (launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s) != cudaSuccess)
+        return BOOST_ERR_CUDA;
+    }
     Ap = ws_at<void>(ws, P.off_Ap);
   }
   void* a = ws_at<void>(ws, P.off_a);
@@ -444,10 +469,21 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   g.out2 = dzs;
   g.ldo = P.kr;
   g.qpart = D.has_norm ? qpart : nullptr;
-  cudaError_t e = launch_gemm(P.bn_down, EPI_DUAL, g, sms, s);
+  cudaError_t e;
+  {
+    ProfScope ps(s, K_DUAL, 2.0 * P.T * P.kr * (P.d + P.n),
+                 2.0 * (P.T * P.d + P.d * P.kr + P.k * P.T * P.n + P.kr * P.n + 2 * P.T * P.kr) +
+                     4.0 * P.T * (P.n_tiles_down + 1));
+    e = launch_gemm(P.bn_down, EPI_DUAL, g, sms, s);
+  }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
   float* part = ws_at<float>(ws, P.off_part);
+  const double wB_flops = 2.0 * P.T * P.kr * P.n;
+  const double wB_bytes = 2.0 * (P.T * P.kr + P.k * P.T * P.n + P.kr * P.n);
+  const double wA_flops = 2.0 * P.T * P.d * P.kr;
+  const double wA_bytes = 2.0 * (P.T * P.d + P.T * P.kr + P.d * P.kr) +
+                          (D.has_norm ? 2.0 * (P.d * P.kr + 2 * P.d) : 0.0);
 
   // K5: dB[i] = a[:, group i]^T @ dy[i]  (M = r, N = n, K = T).
   {
@@ -471,10 +507,17 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.kb_per_split = P.kbps_B;
       w.out = part;
       w.out_sstride = P.k * P.r * P.n;
-      e = launch_gemm(P.bn_wB, EPI_F32, w, sms, s);
-      if (e == cudaSuccess) e = launch_splitk_sum_bf16(part, P.splits_B, P.k * P.r * P.n, dB, s);
+      {
+        ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
+        e = launch_gemm(P.bn_wB, EPI_F32, w, sms, s);
+      }
+      if (e == cudaSuccess) {
+        ProfScope ps(s, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
+        e = launch_splitk_sum_bf16(part, P.splits_B, P.k * P.r * P.n, dB, s);
+      }
     } else {
       w.out = dB;
+      ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
       e = launch_gemm(P.bn_wB, EPI_BF16, w, sms, s);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
@@ -499,18 +542,28 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.kb_per_split = P.kbps_A;
       w.out = part;
       w.out_sstride = P.d * P.kr;
-      e = launch_gemm(P.bn_wA, EPI_F32, w, sms, s);
-      if (e == cudaSuccess)
+      {
+        ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
+        e = launch_gemm(P.bn_wA, EPI_F32, w, sms, s);
+      }
+      if (e == cudaSuccess) {
+        ProfScope ps(s, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
         e = launch_splitk_finalize_dA(part, P.splits_A, P.d, P.kr, D.has_norm ? gamma : nullptr,
                                       A, dA, D.has_norm ? dgamma : nullptr, s);
+      }
     } else {
       w.out = dA;
       w.gamma = D.has_norm ? static_cast<const __nv_bfloat16*>(gamma) : nullptr;
       w.wA = D.has_norm ? static_cast<const __nv_bfloat16*>(A) : nullptr;
       w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
-      e = launch_gemm(P.bn_wA, EPI_DA, w, sms, s);
-      if (e == cudaSuccess && D.has_norm)
+      {
+        ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
+        e = launch_gemm(P.bn_wA, EPI_DA, w, sms, s);
+      }
+      if (e == cudaSuccess && D.has_norm) {
+        ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * w.n_tiles * P.d + 2.0 * P.d);
         e = launch_dgamma_reduce(ws_at<float>(ws, P.off_dg), w.n_tiles, P.d, dgamma, s);
+      }
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
   }
@@ -537,6 +590,9 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.d_norm = static_cast<int32_t>(P.d);
       w.xin = static_cast<const __nv_bfloat16*>(x);
     }
+    ProfScope ps(s, K_DX, 2.0 * P.T * P.kr * P.d,
+                 2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (D.has_norm ? 2 : 1)) +
+                     4.0 * P.T * (P.n_tiles_down + 1));
     e = launch_gemm(P.bn_dx, EPI_DX, w, sms, s);
   }
   return cuda_status(e);
@@ -578,6 +634,7 @@ boost_status boost_swiglu_fwd(int64_t T, int64_t n, const void* gate, const void
   if (T * n == 0) return BOOST_OK;
   boost_status st = check_ptrs({gate, up, h}, {});
   if (st != BOOST_OK) return st;
+  ProfScope ps(static_cast<cudaStream_t>(stream), K_SWIGLU_FWD, 0.0, 6.0 * T * n);
   return cuda_status(launch_swiglu_fwd(gate, up, h, T * n, static_cast<cudaStream_t>(stream)));
 }
 
@@ -588,6 +645,7 @@ boost_status boost_swiglu_bwd(int64_t T, int64_t n, const void* gate, const void
   if (T * n == 0) return BOOST_OK;
   boost_status st = check_ptrs({gate, up, dh, dgate, dup}, {});
   if (st != BOOST_OK) return st;
+  ProfScope ps(static_cast<cudaStream_t>(stream), K_SWIGLU_BWD, 0.0, 10.0 * T * n);
   return cuda_status(
       launch_swiglu_bwd(gate, up, dh, dgate, dup, T * n, static_cast<cudaStream_t>(stream)));
 }
@@ -598,6 +656,7 @@ boost_status boost_add(int64_t count, const void* a, const void* b, void* out, v
   if (count == 0) return BOOST_OK;
   boost_status st = check_ptrs({a, b, out}, {});
   if (st != BOOST_OK) return st;
+  ProfScope ps(static_cast<cudaStream_t>(stream), K_ADD, 0.0, 6.0 * count);
   return cuda_status(launch_add(a, b, out, count, static_cast<cudaStream_t>(stream)));
 }
 

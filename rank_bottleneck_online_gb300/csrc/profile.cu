@@ -1,0 +1,126 @@
+// profile.cu -- optional per-kernel timing of the library's own launches.
+//
+// When enabled, every kernel launch is bracketed by two CUDA events recorded on
+// the launch's stream, and the launch's algorithmic work (flops and bytes, from the
+// shapes) is accumulated per kernel. Reading the counters synchronises the pending
+// events. Disabled (the default), a launch pays one relaxed atomic load.
+#include "profile.h"
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+namespace boost_gb300 {
+
+namespace {
+
+const char* const kNames[K_COUNT] = {
+    "rmsnorm_stats", "fold_gamma",     "gemm_down_act",  "gemm_up",
+    "gemm_dual",     "gemm_wgrad_B",   "gemm_wgrad_A",   "gemm_dx",
+    "splitk_sum",    "splitk_finalize_dA", "dgamma_reduce", "swiglu_fwd",
+    "swiglu_bwd",    "add",            "wait_probe"};
+
+struct Pending {
+  int id;
+  cudaEvent_t e0, e1;
+  double flops, bytes;
+};
+
+struct Totals {
+  int64_t launches = 0;
+  double ms = 0.0, flops = 0.0, bytes = 0.0;
+};
+
+std::atomic<int> g_enabled{0};
+std::mutex g_mu;
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_pool;
+Totals g_tot[K_COUNT];
+
+cudaEvent_t take_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+void drain_locked() {
+  for (Pending& p : g_pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(p.e1) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, p.e0, p.e1) == cudaSuccess) {
+      Totals& t = g_tot[p.id];
+      t.launches += 1;
+      t.ms += ms;
+      t.flops += p.flops;
+      t.bytes += p.bytes;
+    } else {
+      cudaGetLastError();
+    }
+    g_pool.push_back(p.e0);
+    g_pool.push_back(p.e1);
+  }
+  g_pending.clear();
+}
+
+}  // namespace
+
+ProfScope::ProfScope(cudaStream_t s, int id, double flops, double bytes)
+    : stream_(s), id_(id), flops_(flops), bytes_(bytes) {
+  if (g_enabled.load(std::memory_order_relaxed) == 0) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  e0_ = take_event();
+  e1_ = take_event();
+  if (e0_ && e1_) {
+    cudaEventRecord(e0_, stream_);
+    active_ = true;
+  }
+}
+
+ProfScope::~ProfScope() {
+  if (!active_) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaEventRecord(e1_, stream_);
+  g_pending.push_back(Pending{id_, e0_, e1_, flops_, bytes_});
+}
+
+}  // namespace boost_gb300
+
+using namespace boost_gb300;
+
+extern "C" {
+
+boost_status boost_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  drain_locked();
+  if (on) {
+    for (auto& t : g_tot) t = Totals{};
+  }
+  g_enabled.store(on ? 1 : 0);
+  return BOOST_OK;
+}
+
+int boost_profile_kernel_count(void) { return K_COUNT; }
+
+boost_status boost_profile_read(int id, const char** name, int64_t* launches, double* total_ms,
+                                double* total_flops, double* total_bytes) {
+  if (id < 0 || id >= K_COUNT) return BOOST_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  drain_locked();
+  const Totals& t = g_tot[id];
+  if (name) *name = kNames[id];
+  if (launches) *launches = t.launches;
+  if (total_ms) *total_ms = t.ms;
+  if (total_flops) *total_flops = t.flops;
+  if (total_bytes) *total_bytes = t.bytes;
+  return BOOST_OK;
+}
+
+}  // extern "C"

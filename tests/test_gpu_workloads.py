@@ -1,0 +1,104 @@
+"""GPU parity of the composed workloads against the oracle: the LLaMA MLP (gate/up
+bottleneck -> SwiGLU -> down bottleneck), the full layer without its attention
+core, the SVD-style pair, and the full-size LLaMA-2-1B attention-projection
+block.
+"""
+
+import pytest
+import torch
+
+import oracle
+from rank_bottleneck_online_gb300 import binding as B
+from rank_bottleneck_online_gb300 import build as build_mod
+from rank_bottleneck_online_gb300 import inputs
+from rank_bottleneck_online_gb300.block import MLP, Block, Layer, SVDPair
+
+from parity import assert_close, oracle_block
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_mod.build()
+    B.lib()
+
+
+def f64(w, keys):
+    return [inputs.as_f64(w[k]) for k in keys]
+
+
+@pytest.mark.parametrize("T,d,r,ffn,S", [(512, 256, 128, 384, 4), (300, 128, 64, 200, 2)])
+def test_mlp_parity(T, d, r, ffn, S):
+    w = inputs.make_mlp(T, d, r, ffn, seed=1)
+    mlp = MLP(T, d, r, ffn, S=S, weights=w)
+    x, dout = w["x"].cuda(), w["dout"].cuda()
+    out = mlp.forward(x)
+    mlp.backward(x, dout)
+    B.check(mlp.gu.ws)
+    args = f64(w, ("x", "gamma", "A1", "B1", "A2", "B2"))
+    o, _ = oracle.mlp_fwd(*args, S=S)
+    g = oracle.mlp_bwd(*args, inputs.as_f64(w["dout"]), S=S)
+    assert_close("out", out, o)
+    for k, v in mlp.grads().items():
+        assert_close(k, v, g[k])
+
+
+def test_layer_parity():
+    T, d, r, ffn, S = 256, 256, 64, 384, 4
+    w = inputs.make_layer(T, d, r, ffn, seed=2)
+    layer = Layer(T, d, r, ffn, S=S, weights=w["p"])
+    x = w["x"].cuda()
+    out = layer.forward(x)
+    layer.backward(x, w["dout"].cuda(), w["dq"].cuda(), w["dk"].cuda())
+    B.check(layer.qkv.ws)
+    p = {k: inputs.as_f64(v) for k, v in w["p"].items()}
+    xo = inputs.as_f64(w["x"])
+    o, _ = oracle.layer_fwd(xo, p, S=S)
+    g = oracle.layer_bwd(xo, p, *f64(w, ("dout", "dq", "dk")), S=S)
+    assert_close("out", out, o)
+    assert_close("dx", layer.dx, g["dx"])
+    pairs = {"dgamma1": layer.qkv.dgamma, "dA_qkv": layer.qkv.dA, "dB_qkv": layer.qkv.dB,
+             "dA_o": layer.o.dA, "dB_o": layer.o.dB, "dgamma2": layer.mlp.gu.dgamma,
+             "dA_gu": layer.mlp.gu.dA, "dB_gu": layer.mlp.gu.dB, "dA_dn": layer.mlp.dn.dA,
+             "dB_dn": layer.mlp.dn.dB}
+    for k, v in pairs.items():
+        assert_close(k, v, g[k])
+
+
+def test_svd_pair_parity():
+    T, d, r, ffn, S = 256, 256, 64, 320, 4
+    w = inputs.make_svd_pair(T, d, r, ffn, seed=3)
+    pair = SVDPair(T, d, r, ffn, S=S, weights=w["p"])
+    x = w["x"].cuda()
+    yq, yg = pair.forward(x)
+    pair.backward(x, w["dy_qkv"].cuda(), w["dy_gu"].cuda())
+    B.check(pair.qkv.ws)
+    p = {k: inputs.as_f64(v) for k, v in w["p"].items()}
+    xo = inputs.as_f64(w["x"])
+    oq, og = oracle.svd_pair_fwd(xo, p, S=S)
+    g = oracle.svd_pair_bwd(xo, p, *f64(w, ("dy_qkv", "dy_gu")), S=S)
+    assert_close("y_qkv", yq, oq)
+    assert_close("y_gu", yg, og)
+    assert_close("dx", pair.dx, g["dx"])
+    for k, v in {"dgamma_qkv": pair.qkv.dgamma, "dA_qkv": pair.qkv.dA, "dB_qkv": pair.qkv.dB,
+                 "dgamma_gu": pair.gu.dgamma, "dA_gu": pair.gu.dA, "dB_gu": pair.gu.dB}.items():
+        assert_close(k, v, g[k])
+
+
+@pytest.mark.slow
+def test_llama2_1b_attention_block_full_size():
+    c = inputs.CONFIGS["llama2_1b_attn_block"]
+    T, d, r, k, n, S = c["T"], c["d"], c["r"], c["k"], c["n"], c["S"]
+    w = inputs.make_block(T, d, r, k, n, seed=0)
+    blk = Block(T, d, r, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    blk.forward(x)
+    blk.backward(x, dy)
+    B.check(blk.ws)
+    y, _, g = oracle_block(w, act="silu", has_norm=True, S=S)
+    assert_close("y", blk.y, y)
+    for key, got in (("dx", blk.dx), ("dA", blk.dA), ("dB", blk.dB), ("dgamma", blk.dgamma)):
+        assert_close(key, got, g[key])
