@@ -144,6 +144,28 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x,
                                  float* ssq, float* rstd, void* stream);
 
 /*
+ * Row scales without any device allocation. The paper has no counterpart to this
+ * entry point; it exists for callers that cannot call cudaMalloc, such as code
+ * running inside a host framework whose caching allocator owns all device memory
+ * (a direct allocation would bypass its accounting or fail under its memory cap)
+ * and plugins that are handed only their input and output buffers.
+ *   x     [T, d]   input activations (device)
+ *   rstd  [T] fp32 out: (sum_s ssq[s,t] / d + eps)^-1/2, the same value
+ *                  boost_rmsnorm_stats returns; desc->has_norm must be 1
+ * The S x T per-shard partials live in one fixed array of 2^20 floats (4 MiB)
+ * inside the library, reserved on every GPU that loads it and held until the
+ * process exits. Limit: S*T <= 1048576, else BOOST_ERR_UNSUPPORTED_SHAPE and
+ * nothing is enqueued. No call allocates or frees memory. The first call on a
+ * device looks up the array's device address with that device current; make that
+ * first call before any stream capture. All calls share the array (each call
+ * writes every partial it reads, so nothing is cleared and the array keeps the
+ * last call's values): calls whose kernels overlap on the GPU race, so serialise
+ * them (one stream, or events between streams).
+ */
+boost_status boost_rmsnorm_rstd_noalloc(const boost_block_desc* desc, const void* x,
+                                        float* rstd, void* stream);
+
+/*
  * Exact bookkeeping of the shard and group partition (host only, no CUDA).
  *   shard_off       host [S+1]: shard s covers columns [shard_off[s], shard_off[s+1]) of d
  *   group_col_off   host [k+1]: group i covers columns [off[i], off[i+1]) of A

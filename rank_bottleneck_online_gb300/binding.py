@@ -31,7 +31,7 @@ EXPORTS = (
     "boost_rmsnorm_stats", "boost_block_layout", "boost_block_check", "boost_status_string",
     "boost_swiglu_fwd", "boost_swiglu_bwd", "boost_add", "boost_debug_wait_timeout",
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
-    "boost_profile_read",
+    "boost_profile_read", "boost_rmsnorm_rstd_noalloc",
 )
 
 
@@ -82,6 +82,7 @@ def lib():
     L.boost_debug_wait_timeout.argtypes = [vp, sz, u32, vp]
     szp = ctypes.POINTER(sz)
     L.boost_block_ws_layout.argtypes = [dp, szp, szp, szp, szp]
+    L.boost_rmsnorm_rstd_noalloc.argtypes = [dp, vp, vp, vp]
     L.boost_profile_enable.argtypes = [ctypes.c_int]
     L.boost_profile_kernel_count.argtypes = []
     dbl = ctypes.POINTER(ctypes.c_double)
@@ -190,6 +191,18 @@ def rmsnorm_stats(desc: Desc, x, ssq=None, rstd=None, stream=None):
     _check(lib().boost_rmsnorm_stats(ctypes.byref(desc), _ptr(x), _ptr(ssq), _ptr(rstd),
                                      _stream(stream)), "boost_rmsnorm_stats")
     return ssq, rstd
+
+
+def rmsnorm_rstd_noalloc(desc: Desc, x, rstd=None, stream=None):
+    """Row scales through the allocation-free entry point (for callers that cannot
+    allocate device memory; the partials use the library's fixed device array)."""
+    _need(x, "x", torch.bfloat16, (desc.T, desc.d))
+    if rstd is None:
+        rstd = torch.empty(desc.T, dtype=torch.float32, device=x.device)
+    _need(rstd, "rstd", torch.float32, (desc.T,))
+    _check(lib().boost_rmsnorm_rstd_noalloc(ctypes.byref(desc), _ptr(x), _ptr(rstd),
+                                            _stream(stream)), "boost_rmsnorm_rstd_noalloc")
+    return rstd
 
 
 def block_fwd(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=None, stream=None):

@@ -25,7 +25,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libboost_block.so")
 
-SOURCES = ["boost_block.cu", "kernels_simple.cu", "gemm_fwd.cu", "gemm_bwd.cu", "profile.cu"]
+SOURCES = ["boost_block.cu", "kernels_simple.cu", "gemm_fwd.cu", "gemm_bwd.cu", "profile.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
