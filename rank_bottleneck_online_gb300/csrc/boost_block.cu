@@ -21,14 +21,16 @@
 #include "profile.h"
 
 namespace boost_gb300 {
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
                                   cudaStream_t stream);
-cudaError_t launch_gemm_bwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
                                   cudaStream_t stream);
 
-cudaError_t launch_gemm(int bn, int mode, const GemmParams& p, int num_sms, cudaStream_t stream) {
-  if (mode == EPI_ACT || mode == EPI_BF16) return launch_gemm_fwd_modes(bn, mode, p, num_sms, stream);
-  return launch_gemm_bwd_modes(bn, mode, p, num_sms, stream);
+cudaError_t launch_gemm(int bn, int mode, int cg, const GemmParams& p, int num_sms,
+                        cudaStream_t stream) {
+  if (mode == EPI_ACT || mode == EPI_BF16)
+    return launch_gemm_fwd_modes(bn, mode, cg, p, num_sms, stream);
+  return launch_gemm_bwd_modes(bn, mode, cg, p, num_sms, stream);
 }
 }  // namespace boost_gb300
 
@@ -123,16 +125,17 @@ OperandView mnmajor_2d() { return OperandView{0, 1, 2, 1}; }  // (mn, k, -)
 // ------------------------------------------------------------------ plan
 struct Plan {
   int64_t T, d, r, k, n, kr;
-  int bn_down;               // K2 / K4 tile width (grouped tiling over k groups of r)
-  int tiles_per_group;
-  int n_tiles_down;
-  int bn_up, bn_dx;
-  int bn_wB, splits_B, kbps_B;
-  int bn_wA, splits_A, kbps_A;
+  int bn_down, cg_down, tpg_down;   // K2: grouped down-projection (tiles per group)
+  int bn_dual, cg_dual, tpg_dual;   // K4: recompute + dgrad, two accumulators
+  int n_tiles_dual;                 // q partial rows written by K4
+  int bn_up, cg_up;                 // K3
+  int bn_dx, cg_dx;                 // K7
+  int bn_wB, cg_wB, splits_B, kbps_B;
+  int bn_wA, cg_wA, splits_A, kbps_A;
   size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_part, total;
 };
 
-void choose_splits(int64_t tiles, int64_t nkb, int sms, int& splits, int& kbps) {
+void choose_splits(int64_t tiles, int64_t nkb, int groups, int& splits, int& kbps) {
   splits = 1;
   kbps = static_cast<int>(nkb);
   double best = 1e300;
@@ -140,7 +143,7 @@ void choose_splits(int64_t tiles, int64_t nkb, int sms, int& splits, int& kbps) 
     if (s > 1 && nkb / s < 4) break;
     const int64_t per = cdiv(nkb, s);
     const int64_t s_eff = cdiv(nkb, per);
-    const int64_t waves = cdiv(tiles * s_eff, sms);
+    const int64_t waves = cdiv(tiles * s_eff, groups);
     const double cost = static_cast<double>(waves * per) * (s_eff > 1 ? 1.03 : 1.0);
     if (cost < best - 1e-9) {
       best = cost;
@@ -150,23 +153,44 @@ void choose_splits(int64_t tiles, int64_t nkb, int sms, int& splits, int& kbps) 
   }
 }
 
+int env_int(const char* name, int dflt) {
+  const char* e = std::getenv(name);
+  return e ? std::atoi(e) : dflt;
+}
+
+// Tile width for an N extent, and whether a CTA pair (256-row tiles) covers M rows.
+int pick_bn(int64_t n) { return n >= 256 ? 256 : (n >= 128 ? 128 : 64); }
+int pick_cg(int64_t m, int bn) {
+  static const int forced = env_int("BOOST_CG", 0);   // 1 or 2 forces the choice (tuning)
+  if (bn < 128) return 1;
+  if (forced == 1 || forced == 2) return forced;
+  return m >= 256 ? 2 : 1;
+}
+
 Plan make_plan(const boost_block_desc& D, int sms) {
   Plan P{};
   P.T = D.T; P.d = D.d; P.r = D.r; P.k = D.k; P.n = D.n; P.kr = D.k * D.r;
-  P.bn_down = (D.r % 128 == 0) ? 128 : 64;
-  P.tiles_per_group = static_cast<int>(cdiv(D.r, P.bn_down));
-  P.n_tiles_down = static_cast<int>(P.k * P.tiles_per_group);
-  P.bn_up = (D.n >= 256) ? 256 : (D.n > 64 ? 128 : 64);
-  P.bn_dx = (D.d >= 256) ? 256 : (D.d > 64 ? 128 : 64);
-  const int64_t m_tiles_T = cdiv(std::max<int64_t>(D.T, 1), kBM);
+  P.bn_down = pick_bn(D.r);
+  P.cg_down = pick_cg(D.T, P.bn_down);
+  P.tpg_down = static_cast<int>(cdiv(D.r, P.bn_down));
+  static const int dual_bn = env_int("BOOST_DUAL_BN", 256);
+  P.bn_dual = std::min(pick_bn(D.r), dual_bn == 256 ? 256 : (dual_bn == 64 ? 64 : 128));
+  P.cg_dual = pick_cg(D.T, P.bn_dual);
+  P.tpg_dual = static_cast<int>(cdiv(D.r, P.bn_dual));
+  P.n_tiles_dual = static_cast<int>(P.k * P.tpg_dual);
+  P.bn_up = pick_bn(D.n);
+  P.cg_up = pick_cg(D.T, P.bn_up);
+  P.bn_dx = pick_bn(D.d);
+  P.cg_dx = pick_cg(D.T, P.bn_dx);
   const int64_t nkb_T = cdiv(std::max<int64_t>(D.T, 1), kBK);
-  P.bn_wB = (D.n >= 256) ? 256 : (D.n > 64 ? 128 : 64);
-  const int64_t tiles_B = D.k * cdiv(D.r, kBM) * cdiv(D.n, P.bn_wB);
-  choose_splits(tiles_B, nkb_T, sms, P.splits_B, P.kbps_B);
-  P.bn_wA = (P.kr >= 256) ? 256 : (P.kr > 64 ? 128 : 64);
-  const int64_t tiles_A = cdiv(D.d, kBM) * cdiv(P.kr, P.bn_wA);
-  choose_splits(tiles_A, nkb_T, sms, P.splits_A, P.kbps_A);
-  (void)m_tiles_T;
+  P.bn_wB = pick_bn(D.n);
+  P.cg_wB = pick_cg(D.r, P.bn_wB);
+  const int64_t tiles_B = D.k * cdiv(D.r, kBM * P.cg_wB) * cdiv(D.n, P.bn_wB);
+  choose_splits(tiles_B, nkb_T, sms / P.cg_wB, P.splits_B, P.kbps_B);
+  P.bn_wA = pick_bn(P.kr);
+  P.cg_wA = pick_cg(D.d, P.bn_wA);
+  const int64_t tiles_A = cdiv(D.d, kBM * P.cg_wA) * cdiv(P.kr, P.bn_wA);
+  choose_splits(tiles_A, nkb_T, sms / P.cg_wA, P.splits_A, P.kbps_A);
 
   size_t off = align_up(sizeof(DeviceError));
   P.off_rstd = off; off = align_up(off + sizeof(float) * D.T);
@@ -174,7 +198,7 @@ Plan make_plan(const boost_block_desc& D, int sms) {
   P.off_Ap = off;   off = align_up(off + 2ull * D.d * P.kr);
   P.off_a = off;    off = align_up(off + 2ull * D.T * P.kr);
   P.off_dzs = off;  off = align_up(off + 2ull * D.T * P.kr);
-  P.off_q = off;    off = align_up(off + sizeof(float) * P.n_tiles_down * D.T);
+  P.off_q = off;    off = align_up(off + sizeof(float) * P.n_tiles_dual * D.T);
   P.off_dg = off;   off = align_up(off + sizeof(float) * cdiv(P.kr, P.bn_wA) * D.d);
   const size_t partB = P.splits_B > 1 ? sizeof(float) * P.splits_B * D.k * D.r * D.n : 0;
   const size_t partA = P.splits_A > 1 ? sizeof(float) * P.splits_A * D.d * P.kr : 0;
@@ -245,8 +269,9 @@ GemmParams base_params(const Plan& P, DeviceError* err) {
 }
 
 // Down-projection GEMM parameters shared by the forward (K2) and the recompute (K4):
-// M = T, N = k*r tiled per group, K = d; A operand x (K-major), B operand A' (MN-major).
-bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap) {
+// M = T, N = k*r tiled per group (tpg tiles per group), K = d; A operand x (K-major),
+// B operand A' (MN-major).
+bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap, int tpg) {
   if (!map_2d(&g.tmA[0], x, P.T, P.d, 64, kBM)) return false;
   if (!map_2d(&g.tmB[0], Ap, P.d, P.kr, 64, 64)) return false;
   g.seg[0].a = kmajor_2d();
@@ -254,10 +279,9 @@ bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap) {
   g.seg[0].num_kb = static_cast<int32_t>(cdiv(P.d, kBK));
   g.M = static_cast<int32_t>(P.T);
   g.N = static_cast<int32_t>(P.kr);
-  g.m_tiles = static_cast<int32_t>(cdiv(P.T, kBM));
-  g.n_tiles = P.n_tiles_down;
+  g.n_tiles = static_cast<int32_t>(P.k * tpg);
   g.group_n = static_cast<int32_t>(P.r);
-  g.group_tiles = P.tiles_per_group;
+  g.group_tiles = tpg;
   g.m_inner = 0;
   return true;
 }
@@ -362,7 +386,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
 
   // K2: a = act(s * (x @ A')) over all k groups in one GEMM.
   GemmParams g = base_params(P, err);
-  if (!down_segment(g, P, x, Ap)) return BOOST_ERR_CUDA;
+  if (!down_segment(g, P, x, Ap, P.tpg_down)) return BOOST_ERR_CUDA;
   g.act = D.act;
   g.rstd = rs;
   g.out = a;
@@ -371,7 +395,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_DOWN, 2.0 * P.T * P.d * P.kr,
                  2.0 * (P.T * P.d + P.d * P.kr + P.T * P.kr) + 4.0 * P.T);
-    e = launch_gemm(P.bn_down, EPI_ACT, g, sms, s);
+    e = launch_gemm(P.bn_down, EPI_ACT, P.cg_down, g, sms, s);
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
@@ -386,7 +410,6 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   u.M = static_cast<int32_t>(P.T);
   u.N = static_cast<int32_t>(P.n);
   u.batch = static_cast<int32_t>(P.k);
-  u.m_tiles = static_cast<int32_t>(cdiv(P.T, kBM));
   u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.bn_up));
   u.m_inner = 0;
   u.out = y;
@@ -395,7 +418,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
-    e = launch_gemm(P.bn_up, EPI_BF16, u, sms, s);
+    e = launch_gemm(P.bn_up, EPI_BF16, P.cg_up, u, sms, s);
   }
   return cuda_status(e);
 }
@@ -452,10 +475,11 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
 
   // K4: per tile two accumulators, z (recomputed, K = d) and dy_i @ B_i^T (K = n).
   GemmParams g = base_params(P, err);
-  if (!down_segment(g, P, x, Ap)) return BOOST_ERR_CUDA;
+  if (!down_segment(g, P, x, Ap, P.tpg_dual)) return BOOST_ERR_CUDA;
   if (!make_map(&g.tmA[1], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, kBM, 1))
     return BOOST_ERR_CUDA;
-  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, P.bn_down, 1))
+  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, P.bn_dual / P.cg_dual,
+                1))
     return BOOST_ERR_CUDA;
   g.num_seg = 2;
   g.seg[1].a = OperandView{1, 0, 2, 0};   // dy as (n, T, k): K-major, batch = group
@@ -473,8 +497,8 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_DUAL, 2.0 * P.T * P.kr * (P.d + P.n),
                  2.0 * (P.T * P.d + P.d * P.kr + P.k * P.T * P.n + P.kr * P.n + 2 * P.T * P.kr) +
-                     4.0 * P.T * (P.n_tiles_down + 1));
-    e = launch_gemm(P.bn_down, EPI_DUAL, g, sms, s);
+                     4.0 * P.T * (P.n_tiles_dual + 1));
+    e = launch_gemm(P.bn_dual, EPI_DUAL, P.cg_dual, g, sms, s);
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
@@ -497,7 +521,6 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     w.M = static_cast<int32_t>(P.r);
     w.N = static_cast<int32_t>(P.n);
     w.batch = static_cast<int32_t>(P.k);
-    w.m_tiles = static_cast<int32_t>(cdiv(P.r, kBM));
     w.n_tiles = static_cast<int32_t>(cdiv(P.n, P.bn_wB));
     w.m_inner = 1;
     w.ldo = P.n;
@@ -509,7 +532,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.out_sstride = P.k * P.r * P.n;
       {
         ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-        e = launch_gemm(P.bn_wB, EPI_F32, w, sms, s);
+        e = launch_gemm(P.bn_wB, EPI_F32, P.cg_wB, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
@@ -518,7 +541,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     } else {
       w.out = dB;
       ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-      e = launch_gemm(P.bn_wB, EPI_BF16, w, sms, s);
+      e = launch_gemm(P.bn_wB, EPI_BF16, P.cg_wB, w, sms, s);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
   }
@@ -533,7 +556,6 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.T, kBK));
     w.M = static_cast<int32_t>(P.d);
     w.N = static_cast<int32_t>(P.kr);
-    w.m_tiles = static_cast<int32_t>(cdiv(P.d, kBM));
     w.n_tiles = static_cast<int32_t>(cdiv(P.kr, P.bn_wA));
     w.m_inner = 1;
     w.ldo = P.kr;
@@ -544,7 +566,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.out_sstride = P.d * P.kr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.bn_wA, EPI_F32, w, sms, s);
+        e = launch_gemm(P.bn_wA, EPI_F32, P.cg_wA, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
@@ -558,7 +580,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.bn_wA, EPI_DA, w, sms, s);
+        e = launch_gemm(P.bn_wA, EPI_DA, P.cg_wA, w, sms, s);
       }
       if (e == cudaSuccess && D.has_norm) {
         ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * w.n_tiles * P.d + 2.0 * P.d);
@@ -572,13 +594,12 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   {
     GemmParams w = base_params(P, err);
     if (!map_2d(&w.tmA[0], dzs, P.T, P.kr, 64, kBM)) return BOOST_ERR_CUDA;
-    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.bn_dx)) return BOOST_ERR_CUDA;
+    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.bn_dx / P.cg_dx)) return BOOST_ERR_CUDA;
     w.seg[0].a = kmajor_2d();
     w.seg[0].b = kmajor_2d();
     w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.kr, kBK));
     w.M = static_cast<int32_t>(P.T);
     w.N = static_cast<int32_t>(P.d);
-    w.m_tiles = static_cast<int32_t>(cdiv(P.T, kBM));
     w.n_tiles = static_cast<int32_t>(cdiv(P.d, P.bn_dx));
     w.m_inner = 0;
     w.out = dx;
@@ -586,14 +607,14 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     if (D.has_norm) {
       w.rstd = rs;
       w.qpart = qpart;
-      w.nq = P.n_tiles_down;
+      w.nq = P.n_tiles_dual;
       w.d_norm = static_cast<int32_t>(P.d);
       w.xin = static_cast<const __nv_bfloat16*>(x);
     }
     ProfScope ps(s, K_DX, 2.0 * P.T * P.kr * P.d,
                  2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (D.has_norm ? 2 : 1)) +
-                     4.0 * P.T * (P.n_tiles_down + 1));
-    e = launch_gemm(P.bn_dx, EPI_DX, w, sms, s);
+                     4.0 * P.T * (P.n_tiles_dual + 1));
+    e = launch_gemm(P.bn_dx, EPI_DX, P.cg_dx, w, sms, s);
   }
   return cuda_status(e);
 }

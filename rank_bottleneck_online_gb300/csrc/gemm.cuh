@@ -1,13 +1,19 @@
 // gemm.cuh -- persistent, warp-specialised tcgen05 GEMM engine for sm_103a with the
 // bottleneck block's fused epilogues.
 //
-// One CTA per SM walks a static list of output tiles (128 x BN). Roles:
+// One CTA per SM walks a static list of output tiles (128*CG x BN). Roles:
 //   warp 0, lane 0 : TMA producer; fills a ring of shared-memory stages
-//                    (A tile 128x64, B tile BNx64, bf16, 128-byte swizzle)
-//   warp 1         : allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
-//                    into a TMEM accumulator and commits stage/accumulator barriers
+//                    (A tile 128x64, B tile (BN/CG)x64, bf16, 128-byte swizzle)
+//   warp 1         : allocates TMEM; lane 0 (of the even CTA when CG = 2) issues
+//                    tcgen05.mma (M=128*CG, N=BN, K=16) into a TMEM accumulator and
+//                    commits the stage / accumulator barriers
 //   warps 2..5     : epilogue; tcgen05.ld of the accumulator (one TMEM lane quarter
 //                    per warp, one output row per thread), fused math, global stores
+// CG = 2 runs each tile on a CTA pair (a cluster of two SMs, tcgen05 cta_group::2):
+// each SM stages its own 128 rows of A and half of the BN rows of B, so the operand
+// bytes each SM moves per MMA flop are 2/3 of the single-SM tile's. The even CTA
+// issues the MMAs; both CTAs' loads complete on its stage barriers, and its commits
+// are multicast to both CTAs.
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
 // mainloop of tile i+1. Every mbarrier wait is bounded (ptx.cuh).
 //
@@ -29,7 +35,6 @@ constexpr int kBM = 128;           // rows per tile (TMEM lanes)
 constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
 constexpr int kNumThreads = 192;   // 6 warps
-constexpr int kEpiThreads = 128;   // warps 2..5
 
 enum EpiMode : int {
   EPI_ACT = 0,     // out_bf16 = act(s_row * acc)               (down-projection fwd)
@@ -86,13 +91,15 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
-template <int BN, int MODE>
+template <int BN, int MODE, int CG>
 struct GemmCfg {
   static constexpr bool kDual = (MODE == EPI_DUAL);
+  static constexpr int kBRows = BN / CG;                          // B rows staged per CTA
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kAccCols = kDual ? 2 * BN : BN;            // columns per accumulator set
   static constexpr int kAccStages = (2 * kAccCols <= 512) ? 2 : 1;
   static constexpr int kTmemColsRaw = kAccStages * kAccCols;
@@ -100,8 +107,12 @@ struct GemmCfg {
                                    : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAccStages + 1) + 16;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes;
+  static constexpr int kTileM = kBM * CG;
   static_assert(kTmemColsRaw <= 512, "TMEM overflow");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+  static_assert(CG == 1 || CG == 2, "CG is 1 or 2");
+  static_assert(kBRows % 64 == 0, "each CTA stages whole 64-row B boxes");
+  static_assert(kStages >= 3, "pipeline too shallow");
 };
 
 struct TileCoord {
@@ -112,7 +123,7 @@ struct TileCoord {
 
 // Tiles are ordered (split, batch, outer, inner). With group_tiles > 0 the N
 // extent is tiled per group of group_n columns, so no tile straddles two groups.
-template <int BN>
+template <int BN, int TILE_M>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int32_t tile) {
   const int32_t per = p.m_tiles * p.n_tiles;
   const int32_t bs = tile / per;
@@ -128,7 +139,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int32_t ti
   TileCoord c;
   c.split = bs / p.batch;
   c.batch = bs - c.split * p.batch;
-  c.m0 = mb * kBM;
+  c.m0 = mb * TILE_M;
   c.n_blk = nb;
   if (p.group_tiles > 0) {
     c.group = nb / p.group_tiles;
@@ -156,20 +167,30 @@ __device__ __forceinline__ void kb_range(const GemmParams& p, int seg, int32_t s
   }
 }
 
+// Issue the TMA boxes of one operand tile (`rows` MN rows x 64 K) into `dst`.
+// CG = 1 completes on the local barrier `bar`; CG = 2 on the pair barrier at cluster
+// address `bar_cluster` (the even CTA's stage barrier).
+template <int CG>
 __device__ __forceinline__ void load_operand(const CUtensorMap* tm, const OperandView& v,
-                                             uint8_t* dst, uint64_t* bar, int32_t mn, int32_t k,
-                                             int32_t b, int rows) {
+                                             uint8_t* dst, uint64_t* bar, uint32_t bar_cluster,
+                                             int32_t mn, int32_t k, int32_t b, int rows) {
   int32_t c[3] = {0, 0, 0};
   c[v.k_dim] = k;
   c[v.b_dim] = b;
   if (v.mn_major) {
     for (int j = 0; j < rows / 64; ++j) {
       c[v.mn_dim] = mn + 64 * j;
-      tma_load_3d(dst + j * 8192, tm, bar, c[0], c[1], c[2]);
+      if constexpr (CG == 2)
+        tma_load_3d_pair(dst + j * 8192, tm, bar_cluster, c[0], c[1], c[2]);
+      else
+        tma_load_3d(dst + j * 8192, tm, bar, c[0], c[1], c[2]);
     }
   } else {
     c[v.mn_dim] = mn;
-    tma_load_3d(dst, tm, bar, c[0], c[1], c[2]);
+    if constexpr (CG == 2)
+      tma_load_3d_pair(dst, tm, bar_cluster, c[0], c[1], c[2]);
+    else
+      tma_load_3d(dst, tm, bar, c[0], c[1], c[2]);
   }
 }
 
@@ -186,10 +207,154 @@ __device__ __forceinline__ float act_fwd(float z, int act) {
   return z;
 }
 
+// Epilogue of one tile for the calling thread: TMEM lane `row_in_tile` of the
+// accumulator set at column `t_row`, output row `row`, columns [n0, n_end).
 template <int BN, int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
+                                              int32_t row, int32_t n0, int32_t n_end,
+                                              uint32_t t_row) {
+  const bool row_ok = row < p.M;
+  float s_row = 1.0f;
+  if constexpr (MODE == EPI_ACT || MODE == EPI_DUAL || MODE == EPI_DX) {
+    if (p.rstd != nullptr && row_ok) s_row = p.rstd[row];
+  }
+  float rowsum = 0.0f;
+  float coef = 0.0f;
+  if constexpr (MODE == EPI_DX) {
+    if (p.rstd != nullptr && row_ok) {
+      float qs = 0.0f;
+      for (int j = 0; j < p.nq; ++j) qs += p.qpart[static_cast<int64_t>(j) * p.M + row];
+      coef = s_row * s_row * qs / static_cast<float>(p.d_norm);
+    }
+  }
+  float g_row = 1.0f;
+  if constexpr (MODE == EPI_DA) {
+    if (p.gamma != nullptr && row_ok) g_row = __bfloat162float(p.gamma[row]);
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int32_t col0 = n0 + c * 32;
+    float v[32];
+    tmem_ld_32x32b_x32(t_row + c * 32, v);
+    float w[32];
+    if constexpr (MODE == EPI_DUAL) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
+    tmem_ld_wait();
+    if constexpr (MODE == EPI_F32) {
+      if (row_ok) {
+        float* o = static_cast<float*>(p.out) + tc.split * p.out_sstride +
+                   tc.batch * p.out_bstride + static_cast<int64_t>(row) * p.ldo + col0;
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          if (col0 + g * 4 < n_end)
+            *reinterpret_cast<float4*>(o + g * 4) =
+                make_float4(v[g * 4], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+      }
+    } else {
+      uint32_t pk[16];
+      uint32_t pk2[16];
+      if constexpr (MODE == EPI_ACT) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act),
+                              act_fwd(s_row * v[2 * i + 1], p.act));
+      } else if constexpr (MODE == EPI_BF16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      } else if constexpr (MODE == EPI_DUAL) {
+        float a_v[32], dzs_v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float z = s_row * v[i];
+          a_v[i] = act_fwd(z, p.act);   // same expression as EPI_ACT: bitwise recompute
+          float dz;
+          if (p.act == 1) {
+            const float sg = 1.0f / (1.0f + __expf(-z));
+            dz = w[i] * (sg * (1.0f + z * (1.0f - sg)));
+          } else {
+            dz = w[i];
+          }
+          if (col0 + i < n_end) rowsum += dz * z;
+          dzs_v[i] = s_row * dz;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          pk[i] = pack_bf16x2(a_v[2 * i], a_v[2 * i + 1]);
+          pk2[i] = pack_bf16x2(dzs_v[2 * i], dzs_v[2 * i + 1]);
+        }
+      } else if constexpr (MODE == EPI_DX) {
+        float xv[32];
+        if (row_ok && coef != 0.0f) {
+          const uint4* xp = reinterpret_cast<const uint4*>(
+              p.xin + static_cast<int64_t>(row) * p.ldo + col0);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (col0 + g * 8 < n_end) u = xp[g];
+            xv[g * 8 + 0] = bf16_lo(u.x); xv[g * 8 + 1] = bf16_hi(u.x);
+            xv[g * 8 + 2] = bf16_lo(u.y); xv[g * 8 + 3] = bf16_hi(u.y);
+            xv[g * 8 + 4] = bf16_lo(u.z); xv[g * 8 + 5] = bf16_hi(u.z);
+            xv[g * 8 + 6] = bf16_lo(u.w); xv[g * 8 + 7] = bf16_hi(u.w);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) xv[i] = 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(v[2 * i] - coef * xv[2 * i], v[2 * i + 1] - coef * xv[2 * i + 1]);
+      } else if constexpr (MODE == EPI_DA) {
+        if (row_ok && p.wA != nullptr) {
+          const uint4* ap = reinterpret_cast<const uint4*>(
+              p.wA + static_cast<int64_t>(row) * p.ldo + col0);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + g * 8 < n_end) {
+              const uint4 u = ap[g];
+              rowsum += bf16_lo(u.x) * v[g * 8 + 0] + bf16_hi(u.x) * v[g * 8 + 1] +
+                        bf16_lo(u.y) * v[g * 8 + 2] + bf16_hi(u.y) * v[g * 8 + 3] +
+                        bf16_lo(u.z) * v[g * 8 + 4] + bf16_hi(u.z) * v[g * 8 + 5] +
+                        bf16_lo(u.w) * v[g * 8 + 6] + bf16_hi(u.w) * v[g * 8 + 7];
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
+      }
+      if (row_ok) {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
+                           static_cast<int64_t>(row) * p.ldo + col0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          if (col0 + g * 8 < n_end)
+            *reinterpret_cast<uint4*>(o + g * 8) =
+                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        if constexpr (MODE == EPI_DUAL) {
+          __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
+                              static_cast<int64_t>(row) * p.ldo + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (col0 + g * 8 < n_end)
+              *reinterpret_cast<uint4*>(o2 + g * 8) =
+                  make_uint4(pk2[4 * g], pk2[4 * g + 1], pk2[4 * g + 2], pk2[4 * g + 3]);
+        }
+      }
+    }
+  }
+  if constexpr (MODE == EPI_DUAL) {
+    if (row_ok && p.qpart != nullptr)
+      p.qpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
+  }
+  if constexpr (MODE == EPI_DA) {
+    if (row_ok && p.dgpart != nullptr)
+      p.dgpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
+  }
+}
+
+template <int BN, int MODE, int CG>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Cfg = GemmCfg<BN, MODE>;
+  using Cfg = GemmCfg<BN, MODE, CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -204,16 +369,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;   // position in the CTA pair
+  const bool leader = (rank == 0);
   const int32_t num_tiles = p.batch * p.splits * p.m_tiles * p.n_tiles;
+  const int32_t first_tile = static_cast<int32_t>(blockIdx.x) / CG;
+  const int32_t tile_stride = static_cast<int32_t>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], 1);           // the even CTA's expect_tx covers both CTAs
       mbar_init(&empty_bar[s], 1);
     }
     for (int s = 0; s < Cfg::kAccStages; ++s) {
       mbar_init(&tfull_bar[s], 1);
-      mbar_init(&tempty_bar[s], kEpiThreads);
+      mbar_init(&tempty_bar[s], 4 * CG);    // one arrival per epilogue warp of the pair
     }
     mbar_init(done_bar, 1);
     fence_barrier_init();
@@ -227,11 +396,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, Cfg::kTmemCols);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_holder, Cfg::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, Cfg::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -244,8 +418,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool armed[Cfg::kStages];
       for (int s = 0; s < Cfg::kStages; ++s) armed[s] = false, armed_parity[s] = 0;
       bool ok = true;
-      for (int32_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileCoord tc = decode_tile<BN>(p, tile);
+      for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
+        const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
+        const int32_t m_own = tc.m0 + static_cast<int32_t>(rank) * kBM;
+        const int32_t n_half = static_cast<int32_t>(rank) * Cfg::kBRows;
         for (int sg = 0; sg < p.num_seg && ok; ++sg) {
           const Segment& S = p.seg[sg];
           int32_t b = tc.batch;
@@ -259,13 +435,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full_bar[stage], Cfg::kStageBytes);
+            // CG = 2: only the even CTA arms its stage barrier, for both CTAs' bytes; the
+            // odd CTA's copies complete on that barrier too (no cross-CTA arrive, so no
+            // cluster-scope fence per stage).
+            uint32_t bar_cluster = 0;
+            if constexpr (CG == 2) bar_cluster = mapa_shared(smem_u32(&full_bar[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], CG * Cfg::kStageBytes);
             armed[stage] = true;
             armed_parity[stage] = phase;
-            load_operand(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage], tc.m0,
-                         kb * kBK, b, kBM);
-            load_operand(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage], nb,
-                         kb * kBK, b, BN);
+            load_operand<CG>(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage],
+                             bar_cluster, m_own, kb * kBK, b, kBM);
+            load_operand<CG>(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage],
+                             bar_cluster, nb + n_half, kb * kBK, b, Cfg::kBRows);
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -273,14 +454,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
         }
       }
-      // Drain: every copy this thread started has landed before the CTA exits.
-      for (int s = 0; s < Cfg::kStages; ++s) {
-        if (armed[s]) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&full_bar[s], armed_parity[s])) {
-            if (globaltimer_ns() - t0 > p.wait_limit_ns) {
-              record_error(p.err, kErrTimeout, 7);
-              break;
+      // Drain: the copies started here have landed before the CTA exits. Both CTAs'
+      // copies complete on the even CTA's barriers, so the even CTA waits for them.
+      if (leader) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+          if (armed[s]) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&full_bar[s], armed_parity[s])) {
+              if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+                record_error(p.err, kErrTimeout, 7);
+                break;
+              }
             }
           }
         }
@@ -288,7 +472,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -296,9 +480,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       uint32_t idesc[2];
       for (int sg = 0; sg < 2; ++sg)
-        idesc[sg] = idesc_bf16_f32(kBM, BN, p.seg[sg].a.mn_major, p.seg[sg].b.mn_major);
-      for (int32_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileCoord tc = decode_tile<BN>(p, tile);
+        idesc[sg] = idesc_bf16_f32(Cfg::kTileM, BN, p.seg[sg].a.mn_major, p.seg[sg].b.mn_major);
+      for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
+        const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
         if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -319,24 +503,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-              tc_mma_bf16(d_tmem, operand_desc(a_base, a_mn, kk), operand_desc(b_base, b_mn, kk),
-                          idesc[sg], (kb > kb0 || kk > 0) ? 1u : 0u);
+              const uint64_t ad = operand_desc(a_base, a_mn, kk);
+              const uint64_t bd = operand_desc(b_base, b_mn, kk);
+              const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+              if constexpr (CG == 2)
+                tc_mma_bf16_pair(d_tmem, ad, bd, idesc[sg], accum);
+              else
+                tc_mma_bf16(d_tmem, ad, bd, idesc[sg], accum);
             }
-            tc_commit(&empty_bar[stage]);
+            if constexpr (CG == 2) tc_commit_pair_mc(&empty_bar[stage], 0x3);
+            else tc_commit(&empty_bar[stage]);
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
-        tc_commit(&tfull_bar[acc]);
+        if constexpr (CG == 2) tc_commit_pair_mc(&tfull_bar[acc], 0x3);
+        else tc_commit(&tfull_bar[acc]);
         if (++acc == Cfg::kAccStages) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // All MMAs issued by this thread are complete before TMEM is released.
-      tc_commit(done_bar);
+      if constexpr (CG == 2) tc_commit_pair(done_bar); else tc_commit(done_bar);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(done_bar, 0)) {
         if (globaltimer_ns() - t0 > p.wait_limit_ns) {
@@ -351,153 +542,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int32_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const TileCoord tc = decode_tile<BN>(p, tile);
-      const int32_t n0 = tc.n0;
-      const int32_t n_end = tc.n_end;
+    for (int32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
+      const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
       if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
       tc_fence_after();
-      const int32_t row = tc.m0 + row_in_tile;
-      const bool row_ok = row < p.M;
+      const int32_t row = tc.m0 + static_cast<int32_t>(rank) * kBM + row_in_tile;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::kAccCols);
-      float s_row = 1.0f;
-      if constexpr (MODE == EPI_ACT || MODE == EPI_DUAL || MODE == EPI_DX) {
-        if (p.rstd != nullptr && row_ok) s_row = p.rstd[row];
-      }
-      float rowsum = 0.0f;
-      float coef = 0.0f;
-      if constexpr (MODE == EPI_DX) {
-        if (p.rstd != nullptr && row_ok) {
-          float qs = 0.0f;
-          for (int j = 0; j < p.nq; ++j) qs += p.qpart[static_cast<int64_t>(j) * p.M + row];
-          coef = s_row * s_row * qs / static_cast<float>(p.d_norm);
-        }
-      }
-      float g_row = 1.0f;
-      if constexpr (MODE == EPI_DA) {
-        if (p.gamma != nullptr && row_ok) g_row = __bfloat162float(p.gamma[row]);
-      }
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int32_t col0 = n0 + c * 32;
-        float v[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, v);
-        float w[32];
-        if constexpr (MODE == EPI_DUAL) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
-        tmem_ld_wait();
-        if constexpr (MODE == EPI_F32) {
-          if (row_ok) {
-            float* o = static_cast<float*>(p.out) + tc.split * p.out_sstride +
-                       tc.batch * p.out_bstride + static_cast<int64_t>(row) * p.ldo + col0;
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-              if (col0 + g * 4 < n_end)
-                *reinterpret_cast<float4*>(o + g * 4) =
-                    make_float4(v[g * 4], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
-          }
-        } else {
-          uint32_t pk[16];
-          uint32_t pk2[16];
-          if constexpr (MODE == EPI_ACT) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act),
-                                  act_fwd(s_row * v[2 * i + 1], p.act));
-          } else if constexpr (MODE == EPI_BF16) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          } else if constexpr (MODE == EPI_DUAL) {
-            float a_v[32], dzs_v[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float z = s_row * v[i];
-              a_v[i] = act_fwd(z, p.act);   // same expression as EPI_ACT: bitwise recompute
-              float dz;
-              if (p.act == 1) {
-                const float sg = 1.0f / (1.0f + __expf(-z));
-                dz = w[i] * (sg * (1.0f + z * (1.0f - sg)));
-              } else {
-                dz = w[i];
-              }
-              if (col0 + i < n_end) rowsum += dz * z;
-              dzs_v[i] = s_row * dz;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              pk[i] = pack_bf16x2(a_v[2 * i], a_v[2 * i + 1]);
-              pk2[i] = pack_bf16x2(dzs_v[2 * i], dzs_v[2 * i + 1]);
-            }
-          } else if constexpr (MODE == EPI_DX) {
-            float xv[32];
-            if (row_ok && coef != 0.0f) {
-              const uint4* xp = reinterpret_cast<const uint4*>(
-                  p.xin + static_cast<int64_t>(row) * p.ldo + col0);
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (col0 + g * 8 < n_end) u = xp[g];
-                xv[g * 8 + 0] = bf16_lo(u.x); xv[g * 8 + 1] = bf16_hi(u.x);
-                xv[g * 8 + 2] = bf16_lo(u.y); xv[g * 8 + 3] = bf16_hi(u.y);
-                xv[g * 8 + 4] = bf16_lo(u.z); xv[g * 8 + 5] = bf16_hi(u.z);
-                xv[g * 8 + 6] = bf16_lo(u.w); xv[g * 8 + 7] = bf16_hi(u.w);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) xv[i] = 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(v[2 * i] - coef * xv[2 * i], v[2 * i + 1] - coef * xv[2 * i + 1]);
-          } else if constexpr (MODE == EPI_DA) {
-            if (row_ok && p.wA != nullptr) {
-              const uint4* ap = reinterpret_cast<const uint4*>(
-                  p.wA + static_cast<int64_t>(row) * p.ldo + col0);
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                if (col0 + g * 8 < n_end) {
-                  const uint4 u = ap[g];
-                  rowsum += bf16_lo(u.x) * v[g * 8 + 0] + bf16_hi(u.x) * v[g * 8 + 1] +
-                            bf16_lo(u.y) * v[g * 8 + 2] + bf16_hi(u.y) * v[g * 8 + 3] +
-                            bf16_lo(u.z) * v[g * 8 + 4] + bf16_hi(u.z) * v[g * 8 + 5] +
-                            bf16_lo(u.w) * v[g * 8 + 6] + bf16_hi(u.w) * v[g * 8 + 7];
-                }
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
-          }
-          if (row_ok) {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
-                               static_cast<int64_t>(row) * p.ldo + col0;
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-              if (col0 + g * 8 < n_end)
-                *reinterpret_cast<uint4*>(o + g * 8) =
-                    make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-            if constexpr (MODE == EPI_DUAL) {
-              __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
-                                  static_cast<int64_t>(row) * p.ldo + col0;
-#pragma unroll
-              for (int g = 0; g < 4; ++g)
-                if (col0 + g * 8 < n_end)
-                  *reinterpret_cast<uint4*>(o2 + g * 8) =
-                      make_uint4(pk2[4 * g], pk2[4 * g + 1], pk2[4 * g + 2], pk2[4 * g + 3]);
-            }
-          }
-        }
-      }
-      if constexpr (MODE == EPI_DUAL) {
-        if (row_ok && p.qpart != nullptr)
-          p.qpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
-      }
-      if constexpr (MODE == EPI_DA) {
-        if (row_ok && p.dgpart != nullptr)
-          p.dgpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
-      }
+      epilogue_tile<BN, MODE>(p, tc, row, tc.n0, tc.n_end, t_row);
       tc_fence_before();
-      mbar_arrive(&tempty_bar[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        else mbar_arrive(&tempty_bar[acc]);
+      }
       if (++acc == Cfg::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;
@@ -506,10 +564,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) cluster_sync(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    else tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 

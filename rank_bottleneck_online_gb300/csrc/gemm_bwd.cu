@@ -6,25 +6,12 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_bwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
                                   cudaStream_t stream) {
-  if (mode == EPI_DUAL) {
-    if (bn == 64) return launch_one<64, EPI_DUAL>(p, num_sms, stream);
-    if (bn == 128) return launch_one<128, EPI_DUAL>(p, num_sms, stream);
-    if (bn == 256) return launch_one<256, EPI_DUAL>(p, num_sms, stream);
-  } else if (mode == EPI_DX) {
-    if (bn == 64) return launch_one<64, EPI_DX>(p, num_sms, stream);
-    if (bn == 128) return launch_one<128, EPI_DX>(p, num_sms, stream);
-    if (bn == 256) return launch_one<256, EPI_DX>(p, num_sms, stream);
-  } else if (mode == EPI_DA) {
-    if (bn == 64) return launch_one<64, EPI_DA>(p, num_sms, stream);
-    if (bn == 128) return launch_one<128, EPI_DA>(p, num_sms, stream);
-    if (bn == 256) return launch_one<256, EPI_DA>(p, num_sms, stream);
-  } else if (mode == EPI_F32) {
-    if (bn == 64) return launch_one<64, EPI_F32>(p, num_sms, stream);
-    if (bn == 128) return launch_one<128, EPI_F32>(p, num_sms, stream);
-    if (bn == 256) return launch_one<256, EPI_F32>(p, num_sms, stream);
-  }
+  if (mode == EPI_DUAL) return launch_mode<EPI_DUAL>(bn, cg, p, num_sms, stream);
+  if (mode == EPI_DX) return launch_mode<EPI_DX>(bn, cg, p, num_sms, stream);
+  if (mode == EPI_DA) return launch_mode<EPI_DA>(bn, cg, p, num_sms, stream);
+  if (mode == EPI_F32) return launch_mode<EPI_F32>(bn, cg, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -5,17 +5,10 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
                                   cudaStream_t stream) {
-  if (mode == EPI_ACT) {
-    if (bn == 64) return launch_one<64, EPI_ACT>(p, num_sms, stream);
-    if (bn == 128) return launch_one<128, EPI_ACT>(p, num_sms, stream);
-    if (bn == 256) return launch_one<256, EPI_ACT>(p, num_sms, stream);
-  } else if (mode == EPI_BF16) {
-    if (bn == 64) return launch_one<64, EPI_BF16>(p, num_sms, stream);
-    if (bn == 128) return launch_one<128, EPI_BF16>(p, num_sms, stream);
-    if (bn == 256) return launch_one<256, EPI_BF16>(p, num_sms, stream);
-  }
+  if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, p, num_sms, stream);
+  if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -10,8 +10,10 @@
 namespace boost_gb300 {
 
 // ----------------------------------------------------------- GEMM launches
-// Launch gemm_kernel<BN, MODE> persistently on min(tiles, SMs) CTAs.
-cudaError_t launch_gemm(int bn, int mode, const GemmParams& p, int num_sms, cudaStream_t stream);
+// Launch gemm_kernel<BN, MODE, CG> persistently (CG = 2: CTA pairs, 256-row tiles).
+// p.m_tiles is derived from p.M and the tile height.
+cudaError_t launch_gemm(int bn, int mode, int cg, const GemmParams& p, int num_sms,
+                        cudaStream_t stream);
 
 // ------------------------------------------------------ CUDA-core kernels
 cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, float eps,
