@@ -414,9 +414,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed_parity[Cfg::kStages];
-      bool armed[Cfg::kStages];
-      for (int s = 0; s < Cfg::kStages; ++s) armed[s] = false, armed_parity[s] = 0;
+      uint32_t armed_mask = 0, parity_mask = 0;   // per stage: armed, parity of last arm
       bool ok = true;
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
         const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
@@ -441,8 +439,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t bar_cluster = 0;
             if constexpr (CG == 2) bar_cluster = mapa_shared(smem_u32(&full_bar[stage]), 0);
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], CG * Cfg::kStageBytes);
-            armed[stage] = true;
-            armed_parity[stage] = phase;
+            armed_mask |= 1u << stage;
+            parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
             load_operand<CG>(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage],
                              bar_cluster, m_own, kb * kBK, b, kBM);
             load_operand<CG>(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage],
@@ -458,9 +456,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // copies complete on the even CTA's barriers, so the even CTA waits for them.
       if (leader) {
         for (int s = 0; s < Cfg::kStages; ++s) {
-          if (armed[s]) {
+          if (armed_mask & (1u << s)) {
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full_bar[s], armed_parity[s])) {
+            while (!mbar_try_wait(&full_bar[s], (parity_mask >> s) & 1u)) {
               if (globaltimer_ns() - t0 > p.wait_limit_ns) {
                 record_error(p.err, kErrTimeout, 7);
                 break;
@@ -478,9 +476,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      uint32_t idesc[2];
-      for (int sg = 0; sg < 2; ++sg)
-        idesc[sg] = idesc_bf16_f32(Cfg::kTileM, BN, p.seg[sg].a.mn_major, p.seg[sg].b.mn_major);
+      const uint32_t idesc0 =
+          idesc_bf16_f32(Cfg::kTileM, BN, p.seg[0].a.mn_major, p.seg[0].b.mn_major);
+      const uint32_t idesc1 =
+          idesc_bf16_f32(Cfg::kTileM, BN, p.seg[1].a.mn_major, p.seg[1].b.mn_major);
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
         const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
         if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
@@ -491,6 +490,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int sg = 0; sg < p.num_seg && ok; ++sg) {
           const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols + sg * BN;
           const int a_mn = p.seg[sg].a.mn_major, b_mn = p.seg[sg].b.mn_major;
+          const uint32_t idesc = sg == 0 ? idesc0 : idesc1;
           int32_t kb0, kb1;
           kb_range(p, sg, tc.split, kb0, kb1);
           for (int32_t kb = kb0; kb < kb1; ++kb) {
@@ -507,9 +507,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               const uint64_t bd = operand_desc(b_base, b_mn, kk);
               const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
               if constexpr (CG == 2)
-                tc_mma_bf16_pair(d_tmem, ad, bd, idesc[sg], accum);
+                tc_mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
               else
-                tc_mma_bf16(d_tmem, ad, bd, idesc[sg], accum);
+                tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
             }
             if constexpr (CG == 2) tc_commit_pair_mc(&empty_bar[stage], 0x3);
             else tc_commit(&empty_bar[stage]);
