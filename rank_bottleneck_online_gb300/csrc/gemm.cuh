@@ -106,7 +106,9 @@ struct GemmCfg {
   static constexpr int kTmemCols = kTmemColsRaw <= 32 ? 32 : kTmemColsRaw <= 64 ? 64
                                    : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAccStages + 1) + 16;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes;
+  static constexpr int kStgBytes = 4 * 4096;                      // epilogue staging, 4 KB per warp
+  static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 127) / 128 * 128;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStgOffset + kStgBytes;
   static constexpr int kTileM = kBM * CG;
   static_assert(kTmemColsRaw <= 512, "TMEM overflow");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
@@ -202,18 +204,99 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
                   : smem_desc_sw128(base + kk * 32, 16, 1024);
 }
 
+// logistic(z) with the hardware exp2 and a fast reciprocal divide; the rounding of
+// the bf16 results it feeds dominates its few-ulp fp32 error.
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
+
+// The activation of the down-projection epilogue. The forward and the backward's
+// recompute both call this, so the recomputed activation is bitwise the forward one.
 __device__ __forceinline__ float act_fwd(float z, int act) {
-  if (act == 1) return z / (1.0f + __expf(-z));
-  return z;
+  return act == 1 ? z * sigmoid_f(z) : z;
 }
 
-// Epilogue of one tile for the calling thread: TMEM lane `row_in_tile` of the
-// accumulator set at column `t_row`, output row `row`, columns [n0, n_end).
+// ------------------------------------------------------------ staging
+// Each epilogue warp owns a 4 KB shared-memory block through which it turns its
+// row-per-thread accumulator chunk (32 rows x 32 columns) into row-contiguous
+// global accesses. 16-byte chunks are XOR-swizzled by row so that both the
+// row-per-lane side and the contiguous side are free of bank conflicts.
+
+// bf16: row r is 64 B; chunk c of row r sits at chunk slot c ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_store_bf16(uint8_t* stg, int lane, const uint32_t (&pk)[16],
+                                                 __nv_bfloat16* g, int64_t ld, int rows_valid,
+                                                 int cols_valid) {
+  uint4* mine = reinterpret_cast<uint4*>(stg + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    mine[c ^ sw] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2), c = lane & 3;
+    const uint4 v = reinterpret_cast<const uint4*>(stg + r * 64)[c ^ ((r >> 1) & 3)];
+    if (r < rows_valid && c * 8 < cols_valid)
+      *reinterpret_cast<uint4*>(g + static_cast<int64_t>(r) * ld + c * 8) = v;
+  }
+  __syncwarp();
+}
+
+// fp32: row r is 128 B; chunk c of row r sits at chunk slot c ^ (r & 7).
+__device__ __forceinline__ void stage_store_f32(uint8_t* stg, int lane, const float (&v)[32],
+                                                float* g, int64_t ld, int rows_valid,
+                                                int cols_valid) {
+  float4* mine = reinterpret_cast<float4*>(stg + lane * 128);
+  const int sw = lane & 7;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    mine[c ^ sw] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = 4 * j + (lane >> 3), c = lane & 7;
+    const float4 x = reinterpret_cast<const float4*>(stg + r * 128)[c ^ (r & 7)];
+    if (r < rows_valid && c * 4 < cols_valid)
+      *reinterpret_cast<float4*>(g + static_cast<int64_t>(r) * ld + c * 4) = x;
+  }
+  __syncwarp();
+}
+
+// Coalesced read of a 32 x 32 bf16 block (row r at g + r*ld), delivered as this lane's
+// row in fp32; out-of-range rows or columns read as zero.
+__device__ __forceinline__ void stage_load_bf16(uint8_t* stg, int lane, const __nv_bfloat16* g,
+                                                int64_t ld, int rows_valid, int cols_valid,
+                                                float (&out)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2), c = lane & 3;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < rows_valid && c * 8 < cols_valid)
+      v = *reinterpret_cast<const uint4*>(g + static_cast<int64_t>(r) * ld + c * 8);
+    reinterpret_cast<uint4*>(stg + r * 64)[c ^ ((r >> 1) & 3)] = v;
+  }
+  __syncwarp();
+  const uint4* mine = reinterpret_cast<const uint4*>(stg + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = mine[c ^ sw];
+    out[8 * c + 0] = bf16_lo(u.x); out[8 * c + 1] = bf16_hi(u.x);
+    out[8 * c + 2] = bf16_lo(u.y); out[8 * c + 3] = bf16_hi(u.y);
+    out[8 * c + 4] = bf16_lo(u.z); out[8 * c + 5] = bf16_hi(u.z);
+    out[8 * c + 6] = bf16_lo(u.w); out[8 * c + 7] = bf16_hi(u.w);
+  }
+  __syncwarp();
+}
+
+// Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
+// at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
+// Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
 template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
-                                              int32_t row, int32_t n0, int32_t n_end,
-                                              uint32_t t_row) {
+                                              int32_t row0, int32_t n0, int32_t n_end,
+                                              uint32_t t_row, uint8_t* stg, int lane) {
+  const int32_t row = row0 + lane;
   const bool row_ok = row < p.M;
+  const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
   float s_row = 1.0f;
   if constexpr (MODE == EPI_ACT || MODE == EPI_DUAL || MODE == EPI_DX) {
     if (p.rstd != nullptr && row_ok) s_row = p.rstd[row];
@@ -234,24 +317,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int32_t col0 = n0 + c * 32;
+    const int cols_valid = n_end - col0;
+    if (cols_valid <= 0) break;            // warp-uniform: the rest of the tile is outside N
     float v[32];
     tmem_ld_32x32b_x32(t_row + c * 32, v);
     float w[32];
     if constexpr (MODE == EPI_DUAL) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
     tmem_ld_wait();
     if constexpr (MODE == EPI_F32) {
-      if (row_ok) {
-        float* o = static_cast<float*>(p.out) + tc.split * p.out_sstride +
-                   tc.batch * p.out_bstride + static_cast<int64_t>(row) * p.ldo + col0;
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          if (col0 + g * 4 < n_end)
-            *reinterpret_cast<float4*>(o + g * 4) =
-                make_float4(v[g * 4], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
-      }
+      float* o = static_cast<float*>(p.out) + tc.split * p.out_sstride + tc.batch * p.out_bstride +
+                 static_cast<int64_t>(row0) * p.ldo + col0;
+      stage_store_f32(stg, lane, v, o, p.ldo, rows_valid, cols_valid);
     } else {
       uint32_t pk[16];
-      uint32_t pk2[16];
       if constexpr (MODE == EPI_ACT) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -261,40 +339,37 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
       } else if constexpr (MODE == EPI_DUAL) {
-        float a_v[32], dzs_v[32];
+        // a = act(z) (recompute) and dzs = s * act'(z) * (dy B^T); row partial of dz * z.
+        uint32_t pk2[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float z = s_row * v[i];
-          a_v[i] = act_fwd(z, p.act);   // same expression as EPI_ACT: bitwise recompute
-          float dz;
-          if (p.act == 1) {
-            const float sg = 1.0f / (1.0f + __expf(-z));
-            dz = w[i] * (sg * (1.0f + z * (1.0f - sg)));
-          } else {
-            dz = w[i];
+        for (int i = 0; i < 32; i += 2) {
+          float a2[2], d2[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float z = s_row * v[i + h];
+            float dz;
+            if (p.act == 1) {
+              const float sg = sigmoid_f(z);
+              a2[h] = z * sg;
+              dz = w[i + h] * (sg * (1.0f + z * (1.0f - sg)));
+            } else {
+              a2[h] = z;
+              dz = w[i + h];
+            }
+            if (i + h < cols_valid) rowsum += dz * z;
+            d2[h] = s_row * dz;
           }
-          if (col0 + i < n_end) rowsum += dz * z;
-          dzs_v[i] = s_row * dz;
+          pk[i / 2] = pack_bf16x2(a2[0], a2[1]);
+          pk2[i / 2] = pack_bf16x2(d2[0], d2[1]);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          pk[i] = pack_bf16x2(a_v[2 * i], a_v[2 * i + 1]);
-          pk2[i] = pack_bf16x2(dzs_v[2 * i], dzs_v[2 * i + 1]);
-        }
+        __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
+                            static_cast<int64_t>(row0) * p.ldo + col0;
+        stage_store_bf16(stg, lane, pk2, o2, p.ldo, rows_valid, cols_valid);
       } else if constexpr (MODE == EPI_DX) {
         float xv[32];
-        if (row_ok && coef != 0.0f) {
-          const uint4* xp = reinterpret_cast<const uint4*>(
-              p.xin + static_cast<int64_t>(row) * p.ldo + col0);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (col0 + g * 8 < n_end) u = xp[g];
-            xv[g * 8 + 0] = bf16_lo(u.x); xv[g * 8 + 1] = bf16_hi(u.x);
-            xv[g * 8 + 2] = bf16_lo(u.y); xv[g * 8 + 3] = bf16_hi(u.y);
-            xv[g * 8 + 4] = bf16_lo(u.z); xv[g * 8 + 5] = bf16_hi(u.z);
-            xv[g * 8 + 6] = bf16_lo(u.w); xv[g * 8 + 7] = bf16_hi(u.w);
-          }
+        if (__any_sync(0xffffffffu, coef != 0.0f)) {   // warp-uniform: the load is cooperative
+          stage_load_bf16(stg, lane, p.xin + static_cast<int64_t>(row0) * p.ldo + col0, p.ldo,
+                          rows_valid, cols_valid, xv);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) xv[i] = 0.0f;
@@ -303,42 +378,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(v[2 * i] - coef * xv[2 * i], v[2 * i + 1] - coef * xv[2 * i + 1]);
       } else if constexpr (MODE == EPI_DA) {
-        if (row_ok && p.wA != nullptr) {
-          const uint4* ap = reinterpret_cast<const uint4*>(
-              p.wA + static_cast<int64_t>(row) * p.ldo + col0);
+        if (p.wA != nullptr) {
+          float av[32];
+          stage_load_bf16(stg, lane, p.wA + static_cast<int64_t>(row0) * p.ldo + col0, p.ldo,
+                          rows_valid, cols_valid, av);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + g * 8 < n_end) {
-              const uint4 u = ap[g];
-              rowsum += bf16_lo(u.x) * v[g * 8 + 0] + bf16_hi(u.x) * v[g * 8 + 1] +
-                        bf16_lo(u.y) * v[g * 8 + 2] + bf16_hi(u.y) * v[g * 8 + 3] +
-                        bf16_lo(u.z) * v[g * 8 + 4] + bf16_hi(u.z) * v[g * 8 + 5] +
-                        bf16_lo(u.w) * v[g * 8 + 6] + bf16_hi(u.w) * v[g * 8 + 7];
-            }
-          }
+          for (int i = 0; i < 32; ++i) rowsum += av[i] * v[i];
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
       }
-      if (row_ok) {
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
-                           static_cast<int64_t>(row) * p.ldo + col0;
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-          if (col0 + g * 8 < n_end)
-            *reinterpret_cast<uint4*>(o + g * 8) =
-                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-        if constexpr (MODE == EPI_DUAL) {
-          __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
-                              static_cast<int64_t>(row) * p.ldo + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (col0 + g * 8 < n_end)
-              *reinterpret_cast<uint4*>(o2 + g * 8) =
-                  make_uint4(pk2[4 * g], pk2[4 * g + 1], pk2[4 * g + 2], pk2[4 * g + 3]);
-        }
-      }
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
+                         static_cast<int64_t>(row0) * p.ldo + col0;
+      stage_store_bf16(stg, lane, pk, o, p.ldo, rows_valid, cols_valid);
     }
   }
   if constexpr (MODE == EPI_DUAL) {
@@ -539,17 +592,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                    // TMEM lane quarter of this warp
-    const int row_in_tile = q * 32 + lane;
+    uint8_t* stg = smem + Cfg::kStgOffset + (warp - 2) * 4096;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
       const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
       if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
       tc_fence_after();
-      const int32_t row = tc.m0 + static_cast<int32_t>(rank) * kBM + row_in_tile;
+      const int32_t row0 = tc.m0 + static_cast<int32_t>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::kAccCols);
-      epilogue_tile<BN, MODE>(p, tc, row, tc.n0, tc.n_end, t_row);
+      epilogue_tile<BN, MODE>(p, tc, row0, tc.n0, tc.n_end, t_row, stg, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
