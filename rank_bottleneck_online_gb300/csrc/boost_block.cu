@@ -21,16 +21,16 @@
 #include "profile.h"
 
 namespace boost_gb300 {
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
-                                  cudaStream_t stream);
-cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
-                                  cudaStream_t stream);
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p,
+                                  int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p,
+                                  int num_sms, cudaStream_t stream);
 
-cudaError_t launch_gemm(int bn, int mode, int cg, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
                         cudaStream_t stream) {
   if (mode == EPI_ACT || mode == EPI_BF16)
-    return launch_gemm_fwd_modes(bn, mode, cg, p, num_sms, stream);
-  return launch_gemm_bwd_modes(bn, mode, cg, p, num_sms, stream);
+    return launch_gemm_fwd_modes(bn, mode, cg, mc, p, num_sms, stream);
+  return launch_gemm_bwd_modes(bn, mode, cg, mc, p, num_sms, stream);
 }
 }  // namespace boost_gb300
 
@@ -125,17 +125,26 @@ OperandView mnmajor_2d() { return OperandView{0, 1, 2, 1}; }  // (mn, k, -)
 // ------------------------------------------------------------------ plan
 struct Plan {
   int64_t T, d, r, k, n, kr;
-  int bn_down, cg_down, tpg_down;   // K2: grouped down-projection (tiles per group)
-  int bn_dual, cg_dual, tpg_dual;   // K4: recompute + dgrad, two accumulators
-  int n_tiles_dual;                 // q partial rows written by K4
-  int bn_up, cg_up;                 // K3
-  int bn_dx, cg_dx;                 // K7
-  int bn_wB, cg_wB, splits_B, kbps_B;
-  int bn_wA, cg_wA, splits_A, kbps_A;
+  // per GEMM: tile width, CTA-pair (cg = 2) and pairs sharing B by multicast (mc = 2)
+  int bn_down, cg_down, mc_down, tpg_down;   // K2: grouped down-projection (tiles per group)
+  int bn_dual, cg_dual, mc_dual, tpg_dual;   // K4: recompute + dgrad, two accumulators
+  int n_tiles_dual;                          // q partial rows written by K4
+  int bn_up, cg_up, mc_up;                   // K3
+  int bn_dx, cg_dx, mc_dx;                   // K7
+  int bn_wB, cg_wB, mc_wB, splits_B, kbps_B;
+  int bn_wA, cg_wA, mc_wA, splits_A, kbps_A;
   size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_part, total;
 };
 
-void choose_splits(int64_t tiles, int64_t nkb, int groups, int& splits, int& kbps) {
+// Split-K choice for a weight gradient: minimise the estimated time
+//   waves(s) * k-blocks per split * t_kb  +  partial bytes / HBM bandwidth,
+// where a wave is one pass of `groups` CTA groups over the tile list, t_kb is the
+// time of one 64-deep k-block of a 256x256 tile on a CTA pair (about 0.5 us at the
+// measured ~1.2-1.3 PFLOP/s), and the fp32 partials are written once and read once.
+void choose_splits(int64_t tiles, int64_t nkb, int groups, int64_t out_elems, int& splits,
+                   int& kbps) {
+  constexpr double kTkb = 0.5e-6;          // seconds per k-block per tile
+  constexpr double kHbm = 6.0e12;          // bytes per second
   splits = 1;
   kbps = static_cast<int>(nkb);
   double best = 1e300;
@@ -144,8 +153,9 @@ void choose_splits(int64_t tiles, int64_t nkb, int groups, int& splits, int& kbp
     const int64_t per = cdiv(nkb, s);
     const int64_t s_eff = cdiv(nkb, per);
     const int64_t waves = cdiv(tiles * s_eff, groups);
-    const double cost = static_cast<double>(waves * per) * (s_eff > 1 ? 1.03 : 1.0);
-    if (cost < best - 1e-9) {
+    double cost = static_cast<double>(waves * per) * kTkb;
+    if (s_eff > 1) cost += 2.0 * 4.0 * static_cast<double>(s_eff) * out_elems / kHbm;
+    if (cost < best * (1.0 - 1e-6)) {
       best = cost;
       splits = static_cast<int>(s_eff);
       kbps = static_cast<int>(per);
@@ -166,31 +176,44 @@ int pick_cg(int64_t m, int bn) {
   if (forced == 1 || forced == 2) return forced;
   return m >= 256 ? 2 : 1;
 }
+// Two pairs per cluster sharing B by multicast: 256-wide pair tiles with M >= 512.
+int pick_mc(int64_t m, int bn, int cg) {
+  static const int forced = env_int("BOOST_MC", 0);   // 1 disables (tuning)
+  if (cg != 2 || bn != 256 || forced == 1) return 1;
+  return m >= 512 ? 2 : 1;
+}
 
 Plan make_plan(const boost_block_desc& D, int sms) {
   Plan P{};
   P.T = D.T; P.d = D.d; P.r = D.r; P.k = D.k; P.n = D.n; P.kr = D.k * D.r;
   P.bn_down = pick_bn(D.r);
   P.cg_down = pick_cg(D.T, P.bn_down);
+  P.mc_down = pick_mc(D.T, P.bn_down, P.cg_down);
   P.tpg_down = static_cast<int>(cdiv(D.r, P.bn_down));
   static const int dual_bn = env_int("BOOST_DUAL_BN", 256);
   P.bn_dual = std::min(pick_bn(D.r), dual_bn == 256 ? 256 : (dual_bn == 64 ? 64 : 128));
   P.cg_dual = pick_cg(D.T, P.bn_dual);
+  P.mc_dual = pick_mc(D.T, P.bn_dual, P.cg_dual);
   P.tpg_dual = static_cast<int>(cdiv(D.r, P.bn_dual));
   P.n_tiles_dual = static_cast<int>(P.k * P.tpg_dual);
   P.bn_up = pick_bn(D.n);
   P.cg_up = pick_cg(D.T, P.bn_up);
+  P.mc_up = pick_mc(D.T, P.bn_up, P.cg_up);
   P.bn_dx = pick_bn(D.d);
   P.cg_dx = pick_cg(D.T, P.bn_dx);
+  P.mc_dx = pick_mc(D.T, P.bn_dx, P.cg_dx);
   const int64_t nkb_T = cdiv(std::max<int64_t>(D.T, 1), kBK);
   P.bn_wB = pick_bn(D.n);
   P.cg_wB = pick_cg(D.r, P.bn_wB);
-  const int64_t tiles_B = D.k * cdiv(D.r, kBM * P.cg_wB) * cdiv(D.n, P.bn_wB);
-  choose_splits(tiles_B, nkb_T, sms / P.cg_wB, P.splits_B, P.kbps_B);
+  P.mc_wB = pick_mc(D.r, P.bn_wB, P.cg_wB);
+  const int64_t tiles_B = D.k * cdiv(D.r, kBM * P.cg_wB * P.mc_wB) * cdiv(D.n, P.bn_wB);
+  choose_splits(tiles_B, nkb_T, sms / (P.cg_wB * P.mc_wB), D.k * D.r * D.n, P.splits_B,
+                P.kbps_B);
   P.bn_wA = pick_bn(P.kr);
   P.cg_wA = pick_cg(D.d, P.bn_wA);
-  const int64_t tiles_A = cdiv(D.d, kBM * P.cg_wA) * cdiv(P.kr, P.bn_wA);
-  choose_splits(tiles_A, nkb_T, sms / P.cg_wA, P.splits_A, P.kbps_A);
+  P.mc_wA = pick_mc(D.d, P.bn_wA, P.cg_wA);
+  const int64_t tiles_A = cdiv(D.d, kBM * P.cg_wA * P.mc_wA) * cdiv(P.kr, P.bn_wA);
+  choose_splits(tiles_A, nkb_T, sms / (P.cg_wA * P.mc_wA), D.d * P.kr, P.splits_A, P.kbps_A);
 
   size_t off = align_up(sizeof(DeviceError));
   P.off_rstd = off; off = align_up(off + sizeof(float) * D.T);
@@ -395,7 +418,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_DOWN, 2.0 * P.T * P.d * P.kr,
                  2.0 * (P.T * P.d + P.d * P.kr + P.T * P.kr) + 4.0 * P.T);
-    e = launch_gemm(P.bn_down, EPI_ACT, P.cg_down, g, sms, s);
+    e = launch_gemm(P.bn_down, EPI_ACT, P.cg_down, P.mc_down, g, sms, s);
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
@@ -418,7 +441,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
-    e = launch_gemm(P.bn_up, EPI_BF16, P.cg_up, u, sms, s);
+    e = launch_gemm(P.bn_up, EPI_BF16, P.cg_up, P.mc_up, u, sms, s);
   }
   return cuda_status(e);
 }
@@ -478,8 +501,8 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   if (!down_segment(g, P, x, Ap, P.tpg_dual)) return BOOST_ERR_CUDA;
   if (!make_map(&g.tmA[1], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, kBM, 1))
     return BOOST_ERR_CUDA;
-  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, P.bn_dual / P.cg_dual,
-                1))
+  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64,
+                P.bn_dual / (P.cg_dual * P.mc_dual), 1))
     return BOOST_ERR_CUDA;
   g.num_seg = 2;
   g.seg[1].a = OperandView{1, 0, 2, 0};   // dy as (n, T, k): K-major, batch = group
@@ -498,7 +521,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     ProfScope ps(s, K_DUAL, 2.0 * P.T * P.kr * (P.d + P.n),
                  2.0 * (P.T * P.d + P.d * P.kr + P.k * P.T * P.n + P.kr * P.n + 2 * P.T * P.kr) +
                      4.0 * P.T * (P.n_tiles_dual + 1));
-    e = launch_gemm(P.bn_dual, EPI_DUAL, P.cg_dual, g, sms, s);
+    e = launch_gemm(P.bn_dual, EPI_DUAL, P.cg_dual, P.mc_dual, g, sms, s);
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
@@ -532,7 +555,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.out_sstride = P.k * P.r * P.n;
       {
         ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-        e = launch_gemm(P.bn_wB, EPI_F32, P.cg_wB, w, sms, s);
+        e = launch_gemm(P.bn_wB, EPI_F32, P.cg_wB, P.mc_wB, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
@@ -541,7 +564,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     } else {
       w.out = dB;
       ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-      e = launch_gemm(P.bn_wB, EPI_BF16, P.cg_wB, w, sms, s);
+      e = launch_gemm(P.bn_wB, EPI_BF16, P.cg_wB, P.mc_wB, w, sms, s);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
   }
@@ -566,7 +589,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.out_sstride = P.d * P.kr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.bn_wA, EPI_F32, P.cg_wA, w, sms, s);
+        e = launch_gemm(P.bn_wA, EPI_F32, P.cg_wA, P.mc_wA, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
@@ -580,7 +603,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.bn_wA, EPI_DA, P.cg_wA, w, sms, s);
+        e = launch_gemm(P.bn_wA, EPI_DA, P.cg_wA, P.mc_wA, w, sms, s);
       }
       if (e == cudaSuccess && D.has_norm) {
         ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * w.n_tiles * P.d + 2.0 * P.d);
@@ -594,7 +617,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   {
     GemmParams w = base_params(P, err);
     if (!map_2d(&w.tmA[0], dzs, P.T, P.kr, 64, kBM)) return BOOST_ERR_CUDA;
-    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.bn_dx / P.cg_dx)) return BOOST_ERR_CUDA;
+    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.bn_dx / (P.cg_dx * P.mc_dx))) return BOOST_ERR_CUDA;
     w.seg[0].a = kmajor_2d();
     w.seg[0].b = kmajor_2d();
     w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.kr, kBK));
@@ -614,7 +637,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     ProfScope ps(s, K_DX, 2.0 * P.T * P.kr * P.d,
                  2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (D.has_norm ? 2 : 1)) +
                      4.0 * P.T * (P.n_tiles_dual + 1));
-    e = launch_gemm(P.bn_dx, EPI_DX, P.cg_dx, w, sms, s);
+    e = launch_gemm(P.bn_dx, EPI_DX, P.cg_dx, P.mc_dx, w, sms, s);
   }
   return cuda_status(e);
 }

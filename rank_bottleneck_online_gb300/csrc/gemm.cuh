@@ -14,6 +14,10 @@
 // bytes each SM moves per MMA flop are 2/3 of the single-SM tile's. The even CTA
 // issues the MMAs; both CTAs' loads complete on its stage barriers, and its commits
 // are multicast to both CTAs.
+// MC = 2 stacks two pairs along M in a cluster of four: both need the same B rows, so
+// each CTA loads half of its B share and multicasts it to its counterpart in the other
+// pair (a quarter fewer L2->SM bytes per flop); a stage is refilled once both pairs'
+// MMAs have released it.
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
 // mainloop of tile i+1. Every mbarrier wait is bounded (ptx.cuh).
 //
@@ -91,7 +95,7 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
-template <int BN, int MODE, int CG>
+template <int BN, int MODE, int CG, int MC = 1>
 struct GemmCfg {
   static constexpr bool kDual = (MODE == EPI_DUAL);
   static constexpr int kBRows = BN / CG;                          // B rows staged per CTA
@@ -109,10 +113,14 @@ struct GemmCfg {
   static constexpr int kStgBytes = 4 * 4096;                      // epilogue staging, 4 KB per warp
   static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 127) / 128 * 128;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStgOffset + kStgBytes;
-  static constexpr int kTileM = kBM * CG;
+  static constexpr int kMmaM = kBM * CG;                    // M of one tcgen05.mma
+  static constexpr int kTileM = kBM * CG * MC;             // MC pairs stacked along M
+  static constexpr int kCluster = CG * MC;
   static_assert(kTmemColsRaw <= 512, "TMEM overflow");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
   static_assert(CG == 1 || CG == 2, "CG is 1 or 2");
+  static_assert(MC == 1 || (MC == 2 && CG == 2 && BN == 256), "multicast needs 256-wide pair tiles");
+  static_assert(kMmaM == 128 || kMmaM == 256, "tcgen05.mma kind::f16 M is 128 or 256 here");
   static_assert(kBRows % 64 == 0, "each CTA stages whole 64-row B boxes");
   static_assert(kStages >= 3, "pipeline too shallow");
 };
@@ -194,6 +202,18 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* tm, const Operan
     else
       tma_load_3d(dst, tm, bar, c[0], c[1], c[2]);
   }
+}
+
+// MC = 2: one 64-row slice (K-major: a 64 K x 64 row box; MN-major: one 64-wide atom)
+// of this CTA's B rows, multicast to the CTA with the same pair rank in both pairs.
+__device__ __forceinline__ void load_operand_mc(const CUtensorMap* tm, const OperandView& v,
+                                                uint8_t* dst, uint32_t bar_cluster, uint16_t mask,
+                                                int32_t mn, int32_t k, int32_t b) {
+  int32_t c[3] = {0, 0, 0};
+  c[v.k_dim] = k;
+  c[v.b_dim] = b;
+  c[v.mn_dim] = mn;
+  tma_load_3d_pair_mc(dst, tm, bar_cluster, mask, c[0], c[1], c[2]);
 }
 
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
@@ -404,10 +424,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
 }
 
-template <int BN, int MODE, int CG>
+template <int BN, int MODE, int CG, int MC>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Cfg = GemmCfg<BN, MODE, CG>;
+  using Cfg = GemmCfg<BN, MODE, CG, MC>;
+  constexpr int CL = Cfg::kCluster;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -422,16 +443,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;   // position in the CTA pair
+  const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0u;   // rank in the cluster
+  const uint32_t rank = crank % CG;                  // position in the CTA pair
+  const uint32_t pp = crank / CG;                    // pair index in the cluster (MC = 2)
+  const uint32_t leader_rank = pp * CG;              // cluster rank of this pair's even CTA
   const bool leader = (rank == 0);
   const int32_t num_tiles = p.batch * p.splits * p.m_tiles * p.n_tiles;
-  const int32_t first_tile = static_cast<int32_t>(blockIdx.x) / CG;
-  const int32_t tile_stride = static_cast<int32_t>(gridDim.x) / CG;
+  const int32_t first_tile = static_cast<int32_t>(blockIdx.x) / CL;
+  const int32_t tile_stride = static_cast<int32_t>(gridDim.x) / CL;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(&full_bar[s], 1);           // the even CTA's expect_tx covers both CTAs
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], MC);         // freed once every pair sharing the stage is done
     }
     for (int s = 0; s < Cfg::kAccStages; ++s) {
       mbar_init(&tfull_bar[s], 1);
@@ -458,7 +482,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   }
   tc_fence_before();
-  if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+  if constexpr (CL > 1) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -471,7 +495,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
         const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
-        const int32_t m_own = tc.m0 + static_cast<int32_t>(rank) * kBM;
+        const int32_t m_own =
+            tc.m0 + static_cast<int32_t>(pp) * (kBM * CG) + static_cast<int32_t>(rank) * kBM;
         const int32_t n_half = static_cast<int32_t>(rank) * Cfg::kBRows;
         for (int sg = 0; sg < p.num_seg && ok; ++sg) {
           const Segment& S = p.seg[sg];
@@ -490,14 +515,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // odd CTA's copies complete on that barrier too (no cross-CTA arrive, so no
             // cluster-scope fence per stage).
             uint32_t bar_cluster = 0;
-            if constexpr (CG == 2) bar_cluster = mapa_shared(smem_u32(&full_bar[stage]), 0);
+            if constexpr (CG == 2)
+              bar_cluster = mapa_shared(smem_u32(&full_bar[stage]), leader_rank);
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], CG * Cfg::kStageBytes);
             armed_mask |= 1u << stage;
             parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
             load_operand<CG>(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage],
                              bar_cluster, m_own, kb * kBK, b, kBM);
-            load_operand<CG>(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage],
-                             bar_cluster, nb + n_half, kb * kBK, b, Cfg::kBRows);
+            if constexpr (MC == 2) {
+              // both pairs need these B rows: each issues one 64-row slice for both
+              const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + CG)));
+              load_operand_mc(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes + pp * 8192, bar_cluster,
+                              mask, nb + n_half + static_cast<int32_t>(pp) * 64, kb * kBK, b);
+            } else {
+              load_operand<CG>(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage],
+                               bar_cluster, nb + n_half, kb * kBK, b, Cfg::kBRows);
+            }
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -529,10 +562,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // The MMA is 128 x CG rows (one pair); MC pairs of a cluster each issue their own.
       const uint32_t idesc0 =
-          idesc_bf16_f32(Cfg::kTileM, BN, p.seg[0].a.mn_major, p.seg[0].b.mn_major);
+          idesc_bf16_f32(Cfg::kMmaM, BN, p.seg[0].a.mn_major, p.seg[0].b.mn_major);
       const uint32_t idesc1 =
-          idesc_bf16_f32(Cfg::kTileM, BN, p.seg[1].a.mn_major, p.seg[1].b.mn_major);
+          idesc_bf16_f32(Cfg::kMmaM, BN, p.seg[1].a.mn_major, p.seg[1].b.mn_major);
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
         const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
         if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
@@ -564,16 +598,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               else
                 tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
             }
-            if constexpr (CG == 2) tc_commit_pair_mc(&empty_bar[stage], 0x3);
-            else tc_commit(&empty_bar[stage]);
+            if constexpr (CG == 2)
+              tc_commit_pair_mc(&empty_bar[stage], static_cast<uint16_t>((1u << CL) - 1u));
+            else
+              tc_commit(&empty_bar[stage]);
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
-        if constexpr (CG == 2) tc_commit_pair_mc(&tfull_bar[acc], 0x3);
-        else tc_commit(&tfull_bar[acc]);
+        if constexpr (CG == 2)
+          tc_commit_pair_mc(&tfull_bar[acc], static_cast<uint16_t>(0x3u << leader_rank));
+        else
+          tc_commit(&tfull_bar[acc]);
         if (++acc == Cfg::kAccStages) {
           acc = 0;
           acc_phase ^= 1u;
@@ -599,14 +637,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
       if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
       tc_fence_after();
-      const int32_t row0 = tc.m0 + static_cast<int32_t>(rank) * kBM + q * 32;
+      const int32_t row0 = tc.m0 + static_cast<int32_t>(pp) * (kBM * CG) +
+                           static_cast<int32_t>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::kAccCols);
       epilogue_tile<BN, MODE>(p, tc, row0, tc.n0, tc.n_end, t_row, stg, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        if constexpr (CG == 2)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), leader_rank));
         else mbar_arrive(&tempty_bar[acc]);
       }
       if (++acc == Cfg::kAccStages) {
@@ -617,7 +657,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 
   tc_fence_before();
-  if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+  if constexpr (CL > 1) cluster_sync(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);

@@ -5,10 +5,10 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
                                   cudaStream_t stream) {
-  if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, p, num_sms, stream);
-  if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, p, num_sms, stream);
+  if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, mc, p, num_sms, stream);
+  if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, mc, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -10,9 +10,10 @@
 namespace boost_gb300 {
 
 // ----------------------------------------------------------- GEMM launches
-// Launch gemm_kernel<BN, MODE, CG> persistently (CG = 2: CTA pairs, 256-row tiles).
-// p.m_tiles is derived from p.M and the tile height.
-cudaError_t launch_gemm(int bn, int mode, int cg, const GemmParams& p, int num_sms,
+// Launch gemm_kernel<BN, MODE, CG, MC> persistently (CG = 2: CTA pairs, 256-row tiles;
+// MC = 2: two pairs per cluster sharing B by multicast). p.m_tiles is derived from p.M
+// and the tile height.
+cudaError_t launch_gemm(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
                         cudaStream_t stream);
 
 // ------------------------------------------------------ CUDA-core kernels

@@ -297,3 +297,20 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
 }
 
 }  // namespace boost_gb300
+
+namespace boost_gb300 {
+
+// 3-D tiled load multicast to the CTAs in `mask` (same shared-memory offset in each);
+// with cta_group::2 the completion is signalled on the stage barrier of each
+// destination CTA's pair (cluster address `bar` of the issuing pair's even CTA).
+__device__ __forceinline__ void tma_load_3d_pair_mc(void* dst, const void* tmap, uint32_t bar,
+                                                    uint16_t mask, int32_t c0, int32_t c1,
+                                                    int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%4, %5, %6}], [%2], %3;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "h"(mask), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+}  // namespace boost_gb300
