@@ -21,16 +21,24 @@
 #include "profile.h"
 
 namespace boost_gb300 {
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p,
-                                  int num_sms, cudaStream_t stream);
-cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p,
-                                  int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mcm, int mcn,
+                                  const GemmParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mcm, int mcn,
+                                  const GemmParams& p, int num_sms, cudaStream_t stream);
+int gemm_resident_fwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms);
+int gemm_resident_bwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms);
 
-cudaError_t launch_gemm(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
-                        cudaStream_t stream) {
+cudaError_t launch_gemm(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p,
+                        int num_sms, cudaStream_t stream) {
   if (mode == EPI_ACT || mode == EPI_BF16)
-    return launch_gemm_fwd_modes(bn, mode, cg, mc, p, num_sms, stream);
-  return launch_gemm_bwd_modes(bn, mode, cg, mc, p, num_sms, stream);
+    return launch_gemm_fwd_modes(bn, mode, cg, mcm, mcn, p, num_sms, stream);
+  return launch_gemm_bwd_modes(bn, mode, cg, mcm, mcn, p, num_sms, stream);
+}
+
+int gemm_resident(int bn, int mode, int cg, int mcm, int mcn, int num_sms) {
+  if (mode == EPI_ACT || mode == EPI_BF16)
+    return gemm_resident_fwd(bn, mode, cg, mcm, mcn, num_sms);
+  return gemm_resident_bwd(bn, mode, cg, mcm, mcn, num_sms);
 }
 }  // namespace boost_gb300
 
@@ -123,16 +131,23 @@ OperandView kmajor_2d() { return OperandView{1, 0, 2, 0}; }   // (k, mn, -)
 OperandView mnmajor_2d() { return OperandView{0, 1, 2, 1}; }  // (mn, k, -)
 
 // ------------------------------------------------------------------ plan
+// Launch shape of one GEMM: tile width, CTA pair (cg = 2), and pairs per cluster along
+// M (mcm, sharing B) and along N (mcn, sharing A) by multicast.
+struct Shape {
+  int bn, cg, mcm, mcn;
+  int64_t super_m() const { return int64_t{kBM} * cg * mcm; }
+  int64_t super_n() const { return int64_t{bn} * mcn; }
+  int a_rows() const { return kBM / mcn; }          // K-major A box rows per CTA load
+  int b_rows() const { return bn / (cg * mcm); }    // K-major B box rows per CTA load
+};
+
 struct Plan {
   int64_t T, d, r, k, n, kr;
-  // per GEMM: tile width, CTA-pair (cg = 2) and pairs sharing B by multicast (mc = 2)
-  int bn_down, cg_down, mc_down, tpg_down;   // K2: grouped down-projection (tiles per group)
-  int bn_dual, cg_dual, mc_dual, tpg_dual;   // K4: recompute + dgrad, two accumulators
-  int n_tiles_dual;                          // q partial rows written by K4
-  int bn_up, cg_up, mc_up;                   // K3
-  int bn_dx, cg_dx, mc_dx;                   // K7
-  int bn_wB, cg_wB, mc_wB, splits_B, kbps_B;
-  int bn_wA, cg_wA, mc_wA, splits_A, kbps_A;
+  Shape down, dual, up, dx, wB, wA;
+  int tpg_down, tpg_dual;           // super-tiles per group of r columns (K2, K4)
+  int n_cols_dual;                  // BN-wide column tiles of K4 (rows of q partials)
+  int n_cols_wA;                    // BN-wide column tiles of K6 (rows of dgamma partials)
+  int splits_B, kbps_B, splits_A, kbps_A;
   size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_part, total;
 };
 
@@ -168,52 +183,48 @@ int env_int(const char* name, int dflt) {
   return e ? std::atoi(e) : dflt;
 }
 
-// Tile width for an N extent, and whether a CTA pair (256-row tiles) covers M rows.
+// Tile width for an N extent.
 int pick_bn(int64_t n) { return n >= 256 ? 256 : (n >= 128 ? 128 : 64); }
-int pick_cg(int64_t m, int bn) {
-  static const int forced = env_int("BOOST_CG", 0);   // 1 or 2 forces the choice (tuning)
-  if (bn < 128) return 1;
-  if (forced == 1 || forced == 2) return forced;
-  return m >= 256 ? 2 : 1;
-}
-// Two pairs per cluster sharing B by multicast: 256-wide pair tiles with M >= 512.
-int pick_mc(int64_t m, int bn, int cg) {
-  static const int forced = env_int("BOOST_MC", 0);   // 1 disables (tuning)
-  if (cg != 2 || bn != 256 || forced == 1) return 1;
-  return m >= 512 ? 2 : 1;
+
+// Launch shape for an M x N output (N tiled per group of `group` columns when > 0).
+// CTA pairs for M >= 256; two pairs stacked along M sharing B when M >= 512; a 2 x 2
+// arrangement sharing A too when N allows whole 512-wide super-tiles.
+Shape pick_shape(int64_t m, int64_t n, int64_t group, int bn_cap = 256) {
+  static const int forced_cg = env_int("BOOST_CG", 0);   // 1 or 2 forces (tuning)
+  static const int mc_limit = env_int("BOOST_MC", 2);    // 1: none, 2: along M, 4: 2 x 2
+  Shape sh{std::min(pick_bn(group > 0 ? group : n), bn_cap), 1, 1, 1};
+  if (sh.bn >= 128) sh.cg = (forced_cg == 1 || forced_cg == 2) ? forced_cg : (m >= 256 ? 2 : 1);
+  if (sh.cg == 2 && sh.bn == 256 && m >= 512 && mc_limit >= 2) {
+    sh.mcm = 2;
+    const bool n_ok = group > 0 ? (group % 512 == 0) : (n >= 512);
+    if (n_ok && mc_limit >= 4) sh.mcn = 2;
+  }
+  return sh;
 }
 
 Plan make_plan(const boost_block_desc& D, int sms) {
   Plan P{};
   P.T = D.T; P.d = D.d; P.r = D.r; P.k = D.k; P.n = D.n; P.kr = D.k * D.r;
-  P.bn_down = pick_bn(D.r);
-  P.cg_down = pick_cg(D.T, P.bn_down);
-  P.mc_down = pick_mc(D.T, P.bn_down, P.cg_down);
-  P.tpg_down = static_cast<int>(cdiv(D.r, P.bn_down));
+  P.down = pick_shape(D.T, P.kr, D.r);
+  P.tpg_down = static_cast<int>(cdiv(D.r, P.down.super_n()));
   static const int dual_bn = env_int("BOOST_DUAL_BN", 256);
-  P.bn_dual = std::min(pick_bn(D.r), dual_bn == 256 ? 256 : (dual_bn == 64 ? 64 : 128));
-  P.cg_dual = pick_cg(D.T, P.bn_dual);
-  P.mc_dual = pick_mc(D.T, P.bn_dual, P.cg_dual);
-  P.tpg_dual = static_cast<int>(cdiv(D.r, P.bn_dual));
-  P.n_tiles_dual = static_cast<int>(P.k * P.tpg_dual);
-  P.bn_up = pick_bn(D.n);
-  P.cg_up = pick_cg(D.T, P.bn_up);
-  P.mc_up = pick_mc(D.T, P.bn_up, P.cg_up);
-  P.bn_dx = pick_bn(D.d);
-  P.cg_dx = pick_cg(D.T, P.bn_dx);
-  P.mc_dx = pick_mc(D.T, P.bn_dx, P.cg_dx);
+  P.dual = pick_shape(D.T, P.kr, D.r, dual_bn == 256 ? 256 : (dual_bn == 64 ? 64 : 128));
+  P.tpg_dual = static_cast<int>(cdiv(D.r, P.dual.super_n()));
+  P.n_cols_dual = static_cast<int>(P.k * P.tpg_dual * P.dual.mcn);
+  P.up = pick_shape(D.T, D.n, 0);
+  P.dx = pick_shape(D.T, D.d, 0);
   const int64_t nkb_T = cdiv(std::max<int64_t>(D.T, 1), kBK);
-  P.bn_wB = pick_bn(D.n);
-  P.cg_wB = pick_cg(D.r, P.bn_wB);
-  P.mc_wB = pick_mc(D.r, P.bn_wB, P.cg_wB);
-  const int64_t tiles_B = D.k * cdiv(D.r, kBM * P.cg_wB * P.mc_wB) * cdiv(D.n, P.bn_wB);
-  choose_splits(tiles_B, nkb_T, sms / (P.cg_wB * P.mc_wB), D.k * D.r * D.n, P.splits_B,
-                P.kbps_B);
-  P.bn_wA = pick_bn(P.kr);
-  P.cg_wA = pick_cg(D.d, P.bn_wA);
-  P.mc_wA = pick_mc(D.d, P.bn_wA, P.cg_wA);
-  const int64_t tiles_A = cdiv(D.d, kBM * P.cg_wA * P.mc_wA) * cdiv(P.kr, P.bn_wA);
-  choose_splits(tiles_A, nkb_T, sms / (P.cg_wA * P.mc_wA), D.d * P.kr, P.splits_A, P.kbps_A);
+  P.wB = pick_shape(D.r, D.n, 0);
+  const int64_t tiles_B = D.k * cdiv(D.r, P.wB.super_m()) * cdiv(D.n, P.wB.super_n());
+  choose_splits(tiles_B, nkb_T,
+                gemm_resident(P.wB.bn, EPI_F32, P.wB.cg, P.wB.mcm, P.wB.mcn, sms),
+                D.k * D.r * D.n, P.splits_B, P.kbps_B);
+  P.wA = pick_shape(D.d, P.kr, 0);
+  P.n_cols_wA = static_cast<int>(cdiv(P.kr, P.wA.super_n()) * P.wA.mcn);
+  const int64_t tiles_A = cdiv(D.d, P.wA.super_m()) * cdiv(P.kr, P.wA.super_n());
+  choose_splits(tiles_A, nkb_T,
+                gemm_resident(P.wA.bn, EPI_F32, P.wA.cg, P.wA.mcm, P.wA.mcn, sms),
+                D.d * P.kr, P.splits_A, P.kbps_A);
 
   size_t off = align_up(sizeof(DeviceError));
   P.off_rstd = off; off = align_up(off + sizeof(float) * D.T);
@@ -221,8 +232,8 @@ Plan make_plan(const boost_block_desc& D, int sms) {
   P.off_Ap = off;   off = align_up(off + 2ull * D.d * P.kr);
   P.off_a = off;    off = align_up(off + 2ull * D.T * P.kr);
   P.off_dzs = off;  off = align_up(off + 2ull * D.T * P.kr);
-  P.off_q = off;    off = align_up(off + sizeof(float) * P.n_tiles_dual * D.T);
-  P.off_dg = off;   off = align_up(off + sizeof(float) * cdiv(P.kr, P.bn_wA) * D.d);
+  P.off_q = off;    off = align_up(off + sizeof(float) * P.n_cols_dual * D.T);
+  P.off_dg = off;   off = align_up(off + sizeof(float) * P.n_cols_wA * D.d);
   const size_t partB = P.splits_B > 1 ? sizeof(float) * P.splits_B * D.k * D.r * D.n : 0;
   const size_t partA = P.splits_A > 1 ? sizeof(float) * P.splits_A * D.d * P.kr : 0;
   P.off_part = off; off = align_up(off + std::max(partA, partB));
@@ -294,8 +305,9 @@ GemmParams base_params(const Plan& P, DeviceError* err) {
 // Down-projection GEMM parameters shared by the forward (K2) and the recompute (K4):
 // M = T, N = k*r tiled per group (tpg tiles per group), K = d; A operand x (K-major),
 // B operand A' (MN-major).
-bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap, int tpg) {
-  if (!map_2d(&g.tmA[0], x, P.T, P.d, 64, kBM)) return false;
+bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap, const Shape& sh,
+                  int tpg) {
+  if (!map_2d(&g.tmA[0], x, P.T, P.d, 64, sh.a_rows())) return false;
   if (!map_2d(&g.tmB[0], Ap, P.d, P.kr, 64, 64)) return false;
   g.seg[0].a = kmajor_2d();
   g.seg[0].b = mnmajor_2d();
@@ -409,7 +421,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
 
   // K2: a = act(s * (x @ A')) over all k groups in one GEMM.
   GemmParams g = base_params(P, err);
-  if (!down_segment(g, P, x, Ap, P.tpg_down)) return BOOST_ERR_CUDA;
+  if (!down_segment(g, P, x, Ap, P.down, P.tpg_down)) return BOOST_ERR_CUDA;
   g.act = D.act;
   g.rstd = rs;
   g.out = a;
@@ -418,13 +430,14 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_DOWN, 2.0 * P.T * P.d * P.kr,
                  2.0 * (P.T * P.d + P.d * P.kr + P.T * P.kr) + 4.0 * P.T);
-    e = launch_gemm(P.bn_down, EPI_ACT, P.cg_down, P.mc_down, g, sms, s);
+    e = launch_gemm(P.down.bn, EPI_ACT, P.down.cg, P.down.mcm, P.down.mcn, g, sms, s);
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
   // K3: y[i] = a[:, group i] @ B[i], batched over the k groups.
   GemmParams u = base_params(P, err);
-  if (!make_map(&u.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, kBM)) return BOOST_ERR_CUDA;
+  if (!make_map(&u.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, P.up.a_rows()))
+    return BOOST_ERR_CUDA;
   if (!make_map(&u.tmB[0], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, 64, 1))
     return BOOST_ERR_CUDA;
   u.seg[0].a = OperandView{2, 0, 1, 0};   // a as (r, k, T): K-major, batch = group
@@ -433,7 +446,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   u.M = static_cast<int32_t>(P.T);
   u.N = static_cast<int32_t>(P.n);
   u.batch = static_cast<int32_t>(P.k);
-  u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.bn_up));
+  u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.up.super_n()));
   u.m_inner = 0;
   u.out = y;
   u.ldo = P.n;
@@ -441,7 +454,7 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
-    e = launch_gemm(P.bn_up, EPI_BF16, P.cg_up, P.mc_up, u, sms, s);
+    e = launch_gemm(P.up.bn, EPI_BF16, P.up.cg, P.up.mcm, P.up.mcn, u, sms, s);
   }
   return cuda_status(e);
 }
@@ -498,11 +511,10 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
 
   // K4: per tile two accumulators, z (recomputed, K = d) and dy_i @ B_i^T (K = n).
   GemmParams g = base_params(P, err);
-  if (!down_segment(g, P, x, Ap, P.tpg_dual)) return BOOST_ERR_CUDA;
-  if (!make_map(&g.tmA[1], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, kBM, 1))
+  if (!down_segment(g, P, x, Ap, P.dual, P.tpg_dual)) return BOOST_ERR_CUDA;
+  if (!make_map(&g.tmA[1], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, P.dual.a_rows(), 1))
     return BOOST_ERR_CUDA;
-  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64,
-                P.bn_dual / (P.cg_dual * P.mc_dual), 1))
+  if (!make_map(&g.tmB[1], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, P.dual.b_rows(), 1))
     return BOOST_ERR_CUDA;
   g.num_seg = 2;
   g.seg[1].a = OperandView{1, 0, 2, 0};   // dy as (n, T, k): K-major, batch = group
@@ -520,8 +532,8 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   {
     ProfScope ps(s, K_DUAL, 2.0 * P.T * P.kr * (P.d + P.n),
                  2.0 * (P.T * P.d + P.d * P.kr + P.k * P.T * P.n + P.kr * P.n + 2 * P.T * P.kr) +
-                     4.0 * P.T * (P.n_tiles_dual + 1));
-    e = launch_gemm(P.bn_dual, EPI_DUAL, P.cg_dual, P.mc_dual, g, sms, s);
+                     4.0 * P.T * (P.n_cols_dual + 1));
+    e = launch_gemm(P.dual.bn, EPI_DUAL, P.dual.cg, P.dual.mcm, P.dual.mcn, g, sms, s);
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
@@ -544,7 +556,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     w.M = static_cast<int32_t>(P.r);
     w.N = static_cast<int32_t>(P.n);
     w.batch = static_cast<int32_t>(P.k);
-    w.n_tiles = static_cast<int32_t>(cdiv(P.n, P.bn_wB));
+    w.n_tiles = static_cast<int32_t>(cdiv(P.n, P.wB.super_n()));
     w.m_inner = 1;
     w.ldo = P.n;
     w.out_bstride = P.r * P.n;
@@ -555,7 +567,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.out_sstride = P.k * P.r * P.n;
       {
         ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-        e = launch_gemm(P.bn_wB, EPI_F32, P.cg_wB, P.mc_wB, w, sms, s);
+        e = launch_gemm(P.wB.bn, EPI_F32, P.wB.cg, P.wB.mcm, P.wB.mcn, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
@@ -564,7 +576,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     } else {
       w.out = dB;
       ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-      e = launch_gemm(P.bn_wB, EPI_BF16, P.cg_wB, P.mc_wB, w, sms, s);
+      e = launch_gemm(P.wB.bn, EPI_BF16, P.wB.cg, P.wB.mcm, P.wB.mcn, w, sms, s);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
   }
@@ -579,7 +591,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.T, kBK));
     w.M = static_cast<int32_t>(P.d);
     w.N = static_cast<int32_t>(P.kr);
-    w.n_tiles = static_cast<int32_t>(cdiv(P.kr, P.bn_wA));
+    w.n_tiles = static_cast<int32_t>(cdiv(P.kr, P.wA.super_n()));
     w.m_inner = 1;
     w.ldo = P.kr;
     if (P.splits_A > 1) {
@@ -589,7 +601,7 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.out_sstride = P.d * P.kr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.bn_wA, EPI_F32, P.cg_wA, P.mc_wA, w, sms, s);
+        e = launch_gemm(P.wA.bn, EPI_F32, P.wA.cg, P.wA.mcm, P.wA.mcn, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
@@ -603,11 +615,11 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.bn_wA, EPI_DA, P.cg_wA, P.mc_wA, w, sms, s);
+        e = launch_gemm(P.wA.bn, EPI_DA, P.wA.cg, P.wA.mcm, P.wA.mcn, w, sms, s);
       }
       if (e == cudaSuccess && D.has_norm) {
-        ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * w.n_tiles * P.d + 2.0 * P.d);
-        e = launch_dgamma_reduce(ws_at<float>(ws, P.off_dg), w.n_tiles, P.d, dgamma, s);
+        ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * P.n_cols_wA * P.d + 2.0 * P.d);
+        e = launch_dgamma_reduce(ws_at<float>(ws, P.off_dg), P.n_cols_wA, P.d, dgamma, s);
       }
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
@@ -616,28 +628,28 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
   // K7: dx = dzs @ A'^T - (s^2 q / d) x  (M = T, N = d, K = k*r).
   {
     GemmParams w = base_params(P, err);
-    if (!map_2d(&w.tmA[0], dzs, P.T, P.kr, 64, kBM)) return BOOST_ERR_CUDA;
-    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.bn_dx / (P.cg_dx * P.mc_dx))) return BOOST_ERR_CUDA;
+    if (!map_2d(&w.tmA[0], dzs, P.T, P.kr, 64, P.dx.a_rows())) return BOOST_ERR_CUDA;
+    if (!map_2d(&w.tmB[0], Ap, P.d, P.kr, 64, P.dx.b_rows())) return BOOST_ERR_CUDA;
     w.seg[0].a = kmajor_2d();
     w.seg[0].b = kmajor_2d();
     w.seg[0].num_kb = static_cast<int32_t>(cdiv(P.kr, kBK));
     w.M = static_cast<int32_t>(P.T);
     w.N = static_cast<int32_t>(P.d);
-    w.n_tiles = static_cast<int32_t>(cdiv(P.d, P.bn_dx));
+    w.n_tiles = static_cast<int32_t>(cdiv(P.d, P.dx.super_n()));
     w.m_inner = 0;
     w.out = dx;
     w.ldo = P.d;
     if (D.has_norm) {
       w.rstd = rs;
       w.qpart = qpart;
-      w.nq = P.n_tiles_dual;
+      w.nq = P.n_cols_dual;
       w.d_norm = static_cast<int32_t>(P.d);
       w.xin = static_cast<const __nv_bfloat16*>(x);
     }
     ProfScope ps(s, K_DX, 2.0 * P.T * P.kr * P.d,
                  2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (D.has_norm ? 2 : 1)) +
-                     4.0 * P.T * (P.n_tiles_dual + 1));
-    e = launch_gemm(P.bn_dx, EPI_DX, P.cg_dx, P.mc_dx, w, sms, s);
+                     4.0 * P.T * (P.n_cols_dual + 1));
+    e = launch_gemm(P.dx.bn, EPI_DX, P.dx.cg, P.dx.mcm, P.dx.mcn, w, sms, s);
   }
   return cuda_status(e);
 }

@@ -14,10 +14,12 @@
 // bytes each SM moves per MMA flop are 2/3 of the single-SM tile's. The even CTA
 // issues the MMAs; both CTAs' loads complete on its stage barriers, and its commits
 // are multicast to both CTAs.
-// MC = 2 stacks two pairs along M in a cluster of four: both need the same B rows, so
-// each CTA loads half of its B share and multicasts it to its counterpart in the other
-// pair (a quarter fewer L2->SM bytes per flop); a stage is refilled once both pairs'
-// MMAs have released it.
+// MCM x MCN pairs form one cluster (2, 4 or 8 CTAs) covering a (256*MCM) x (BN*MCN)
+// super-tile. Pairs in the same column (along M) need the same B rows and pairs in the
+// same row (along N) the same A rows, so each CTA loads one 64-row slice of its shared
+// operand and multicasts it to the CTAs that share it: MCM = 2 saves a quarter and
+// MCM = MCN = 2 half of the L2->SM bytes per MMA flop. A stage is refilled once every
+// pair of the cluster has released it.
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
 // mainloop of tile i+1. Every mbarrier wait is bounded (ptx.cuh).
 //
@@ -95,7 +97,7 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
-template <int BN, int MODE, int CG, int MC = 1>
+template <int BN, int MODE, int CG, int MCM = 1, int MCN = 1>
 struct GemmCfg {
   static constexpr bool kDual = (MODE == EPI_DUAL);
   static constexpr int kBRows = BN / CG;                          // B rows staged per CTA
@@ -114,12 +116,15 @@ struct GemmCfg {
   static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 127) / 128 * 128;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStgOffset + kStgBytes;
   static constexpr int kMmaM = kBM * CG;                    // M of one tcgen05.mma
-  static constexpr int kTileM = kBM * CG * MC;             // MC pairs stacked along M
-  static constexpr int kCluster = CG * MC;
+  static constexpr int kPairs = MCM * MCN;                  // pairs per cluster
+  static constexpr int kTileM = kBM * CG * MCM;            // super-tile rows
+  static constexpr int kTileN = BN * MCN;                  // super-tile columns
+  static constexpr int kCluster = CG * kPairs;
   static_assert(kTmemColsRaw <= 512, "TMEM overflow");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
   static_assert(CG == 1 || CG == 2, "CG is 1 or 2");
-  static_assert(MC == 1 || (MC == 2 && CG == 2 && BN == 256), "multicast needs 256-wide pair tiles");
+  static_assert(kPairs == 1 || (CG == 2 && BN == 256 && MCM <= 2 && MCN <= 2),
+                "multicast needs 256-wide pair tiles");
   static_assert(kMmaM == 128 || kMmaM == 256, "tcgen05.mma kind::f16 M is 128 or 256 here");
   static_assert(kBRows % 64 == 0, "each CTA stages whole 64-row B boxes");
   static_assert(kStages >= 3, "pipeline too shallow");
@@ -204,8 +209,8 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* tm, const Operan
   }
 }
 
-// MC = 2: one 64-row slice (K-major: a 64 K x 64 row box; MN-major: one 64-wide atom)
-// of this CTA's B rows, multicast to the CTA with the same pair rank in both pairs.
+// One 64-row slice (K-major: a 64 K x 64 row box; MN-major: one 64-wide atom) of an
+// operand shared by two pairs, multicast to the CTAs in `mask`.
 __device__ __forceinline__ void load_operand_mc(const CUtensorMap* tm, const OperandView& v,
                                                 uint8_t* dst, uint32_t bar_cluster, uint16_t mask,
                                                 int32_t mn, int32_t k, int32_t b) {
@@ -310,10 +315,12 @@ __device__ __forceinline__ void stage_load_bf16(uint8_t* stg, int lane, const __
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
+// `col_tile` indexes the per-row partial sums (q, dgamma) of this BN-wide column tile.
 template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
                                               int32_t row0, int32_t n0, int32_t n_end,
-                                              uint32_t t_row, uint8_t* stg, int lane) {
+                                              uint32_t t_row, uint8_t* stg, int lane,
+                                              int32_t col_tile) {
   const int32_t row = row0 + lane;
   const bool row_ok = row < p.M;
   const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
@@ -416,18 +423,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
   if constexpr (MODE == EPI_DUAL) {
     if (row_ok && p.qpart != nullptr)
-      p.qpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
+      p.qpart[static_cast<int64_t>(col_tile) * p.M + row] = rowsum;
   }
   if constexpr (MODE == EPI_DA) {
     if (row_ok && p.dgpart != nullptr)
-      p.dgpart[static_cast<int64_t>(tc.n_blk) * p.M + row] = rowsum;
+      p.dgpart[static_cast<int64_t>(col_tile) * p.M + row] = rowsum;
   }
 }
 
-template <int BN, int MODE, int CG, int MC>
+template <int BN, int MODE, int CG, int MCM, int MCN>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Cfg = GemmCfg<BN, MODE, CG, MC>;
+  using Cfg = GemmCfg<BN, MODE, CG, MCM, MCN>;
   constexpr int CL = Cfg::kCluster;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -445,7 +452,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0u;   // rank in the cluster
   const uint32_t rank = crank % CG;                  // position in the CTA pair
-  const uint32_t pp = crank / CG;                    // pair index in the cluster (MC = 2)
+  const uint32_t pp = crank / CG;                    // pair index in the cluster
+  const uint32_t pm = pp % MCM;                      // the pair's row in the super-tile
+  const uint32_t pn = pp / MCM;                      // the pair's column in the super-tile
   const uint32_t leader_rank = pp * CG;              // cluster rank of this pair's even CTA
   const bool leader = (rank == 0);
   const int32_t num_tiles = p.batch * p.splits * p.m_tiles * p.n_tiles;
@@ -455,7 +464,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(&full_bar[s], 1);           // the even CTA's expect_tx covers both CTAs
-      mbar_init(&empty_bar[s], MC);         // freed once every pair sharing the stage is done
+      mbar_init(&empty_bar[s], Cfg::kPairs);  // freed once every pair of the cluster is done
     }
     for (int s = 0; s < Cfg::kAccStages; ++s) {
       mbar_init(&tfull_bar[s], 1);
@@ -494,10 +503,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t armed_mask = 0, parity_mask = 0;   // per stage: armed, parity of last arm
       bool ok = true;
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
-        const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
+        const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
         const int32_t m_own =
-            tc.m0 + static_cast<int32_t>(pp) * (kBM * CG) + static_cast<int32_t>(rank) * kBM;
-        const int32_t n_half = static_cast<int32_t>(rank) * Cfg::kBRows;
+            tc.m0 + static_cast<int32_t>(pm) * (kBM * CG) + static_cast<int32_t>(rank) * kBM;
+        const int32_t n_half = static_cast<int32_t>(pn) * BN + static_cast<int32_t>(rank) * Cfg::kBRows;
         for (int sg = 0; sg < p.num_seg && ok; ++sg) {
           const Segment& S = p.seg[sg];
           int32_t b = tc.batch;
@@ -520,13 +529,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], CG * Cfg::kStageBytes);
             armed_mask |= 1u << stage;
             parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
-            load_operand<CG>(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage],
-                             bar_cluster, m_own, kb * kBK, b, kBM);
-            if constexpr (MC == 2) {
-              // both pairs need these B rows: each issues one 64-row slice for both
-              const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + CG)));
-              load_operand_mc(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes + pp * 8192, bar_cluster,
-                              mask, nb + n_half + static_cast<int32_t>(pp) * 64, kb * kBK, b);
+            if constexpr (MCN == 2) {
+              // the pairs of this row need the same A rows: each issues one 64-row slice
+              uint16_t mask = 0;
+              for (uint32_t j = 0; j < MCN; ++j) mask |= 1u << ((j * MCM + pm) * CG + rank);
+              load_operand_mc(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes + pn * 8192, bar_cluster,
+                              mask, m_own + static_cast<int32_t>(pn) * 64, kb * kBK, b);
+            } else {
+              load_operand<CG>(&p.tmA[sg], S.a, sA + stage * Cfg::kABytes, &full_bar[stage],
+                               bar_cluster, m_own, kb * kBK, b, kBM);
+            }
+            if constexpr (MCM == 2) {
+              // the pairs of this column need the same B rows: each issues one 64-row slice
+              uint16_t mask = 0;
+              for (uint32_t i = 0; i < MCM; ++i) mask |= 1u << ((pn * MCM + i) * CG + rank);
+              load_operand_mc(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes + pm * 8192, bar_cluster,
+                              mask, nb + n_half + static_cast<int32_t>(pm) * 64, kb * kBK, b);
             } else {
               load_operand<CG>(&p.tmB[sg], S.b, sB + stage * Cfg::kBBytes, &full_bar[stage],
                                bar_cluster, nb + n_half, kb * kBK, b, Cfg::kBRows);
@@ -562,13 +580,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      // The MMA is 128 x CG rows (one pair); MC pairs of a cluster each issue their own.
+      // The MMA is 128 x CG rows (one pair); every pair of a cluster issues its own.
       const uint32_t idesc0 =
           idesc_bf16_f32(Cfg::kMmaM, BN, p.seg[0].a.mn_major, p.seg[0].b.mn_major);
       const uint32_t idesc1 =
           idesc_bf16_f32(Cfg::kMmaM, BN, p.seg[1].a.mn_major, p.seg[1].b.mn_major);
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
-        const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
+        const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
         if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -634,14 +652,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
-      const TileCoord tc = decode_tile<BN, Cfg::kTileM>(p, tile);
+      const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
       if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
       tc_fence_after();
-      const int32_t row0 = tc.m0 + static_cast<int32_t>(pp) * (kBM * CG) +
+      const int32_t row0 = tc.m0 + static_cast<int32_t>(pm) * (kBM * CG) +
                            static_cast<int32_t>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::kAccCols);
-      epilogue_tile<BN, MODE>(p, tc, row0, tc.n0, tc.n_end, t_row, stg, lane);
+      // this pair's columns of the super-tile (may be empty past the group or N end)
+      const int32_t pn0 = tc.n0 + static_cast<int32_t>(pn) * BN;
+      const int32_t pend = min(pn0 + BN, tc.n_end);
+      epilogue_tile<BN, MODE>(p, tc, row0, pn0, pend, t_row, stg, lane,
+                              tc.n_blk * MCN + static_cast<int32_t>(pn));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

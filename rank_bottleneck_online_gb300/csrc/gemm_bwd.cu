@@ -6,13 +6,21 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p, int num_sms,
                                   cudaStream_t stream) {
-  if (mode == EPI_DUAL) return launch_mode<EPI_DUAL>(bn, cg, mc, p, num_sms, stream);
-  if (mode == EPI_DX) return launch_mode<EPI_DX>(bn, cg, mc, p, num_sms, stream);
-  if (mode == EPI_DA) return launch_mode<EPI_DA>(bn, cg, mc, p, num_sms, stream);
-  if (mode == EPI_F32) return launch_mode<EPI_F32>(bn, cg, mc, p, num_sms, stream);
+  if (mode == EPI_DUAL) return launch_mode<EPI_DUAL>(bn, cg, mcm, mcn, p, num_sms, stream);
+  if (mode == EPI_DX) return launch_mode<EPI_DX>(bn, cg, mcm, mcn, p, num_sms, stream);
+  if (mode == EPI_DA) return launch_mode<EPI_DA>(bn, cg, mcm, mcn, p, num_sms, stream);
+  if (mode == EPI_F32) return launch_mode<EPI_F32>(bn, cg, mcm, mcn, p, num_sms, stream);
   return cudaErrorInvalidValue;
+}
+
+int gemm_resident_bwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms) {
+  if (mode == EPI_DUAL) return resident_mode<EPI_DUAL>(bn, cg, mcm, mcn, num_sms);
+  if (mode == EPI_DX) return resident_mode<EPI_DX>(bn, cg, mcm, mcn, num_sms);
+  if (mode == EPI_DA) return resident_mode<EPI_DA>(bn, cg, mcm, mcn, num_sms);
+  if (mode == EPI_F32) return resident_mode<EPI_F32>(bn, cg, mcm, mcn, num_sms);
+  return num_sms / cg;
 }
 
 }  // namespace boost_gb300

@@ -5,11 +5,17 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p, int num_sms,
                                   cudaStream_t stream) {
-  if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, mc, p, num_sms, stream);
-  if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, mc, p, num_sms, stream);
+  if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, mcm, mcn, p, num_sms, stream);
+  if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, mcm, mcn, p, num_sms, stream);
   return cudaErrorInvalidValue;
+}
+
+int gemm_resident_fwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms) {
+  if (mode == EPI_ACT) return resident_mode<EPI_ACT>(bn, cg, mcm, mcn, num_sms);
+  if (mode == EPI_BF16) return resident_mode<EPI_BF16>(bn, cg, mcm, mcn, num_sms);
+  return num_sms / cg;
 }
 
 }  // namespace boost_gb300

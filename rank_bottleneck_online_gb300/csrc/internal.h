@@ -10,11 +10,14 @@
 namespace boost_gb300 {
 
 // ----------------------------------------------------------- GEMM launches
-// Launch gemm_kernel<BN, MODE, CG, MC> persistently (CG = 2: CTA pairs, 256-row tiles;
-// MC = 2: two pairs per cluster sharing B by multicast). p.m_tiles is derived from p.M
-// and the tile height.
-cudaError_t launch_gemm(int bn, int mode, int cg, int mc, const GemmParams& p, int num_sms,
-                        cudaStream_t stream);
+// Launch gemm_kernel<BN, MODE, CG, MCM, MCN> persistently (CG = 2: CTA pairs, 256-row
+// tiles; MCM x MCN pairs per cluster sharing B along M and A along N by multicast).
+// p.m_tiles is derived from p.M and the super-tile height; p.n_tiles must count
+// super-tile columns (BN * MCN wide).
+cudaError_t launch_gemm(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p,
+                        int num_sms, cudaStream_t stream);
+// Clusters of that configuration resident at once (the persistent grid size).
+int gemm_resident(int bn, int mode, int cg, int mcm, int mcn, int num_sms);
 
 // ------------------------------------------------------ CUDA-core kernels
 cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, float eps,
