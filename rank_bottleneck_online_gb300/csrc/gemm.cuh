@@ -585,6 +585,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           idesc_bf16_f32(Cfg::kMmaM, BN, p.seg[0].a.mn_major, p.seg[0].b.mn_major);
       const uint32_t idesc1 =
           idesc_bf16_f32(Cfg::kMmaM, BN, p.seg[1].a.mn_major, p.seg[1].b.mn_major);
+      // Shared-memory offsets below 256 KB: the 14-bit start-address field (16 B units)
+      // holds every stage address plus three K steps without carrying into the next field.
+      const uint32_t sA_u32 = smem_u32(sA);
+      const uint32_t sB_u32 = smem_u32(sB);
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
         const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
         if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
@@ -596,6 +600,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols + sg * BN;
           const int a_mn = p.seg[sg].a.mn_major, b_mn = p.seg[sg].b.mn_major;
           const uint32_t idesc = sg == 0 ? idesc0 : idesc1;
+          // Descriptor bits other than the start address are fixed per segment; a K step
+          // of 16 advances the start address by 32 B (K-major) or 2048 B (MN-major).
+          const uint64_t a_hi = desc_hi_sw128(a_mn ? 8192u : 16u, 1024u);
+          const uint64_t b_hi = desc_hi_sw128(b_mn ? 8192u : 16u, 1024u);
+          const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
+          const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
           int32_t kb0, kb1;
           kb_range(p, sg, tc.split, kb0, kb1);
           for (int32_t kb = kb0; kb < kb1; ++kb) {
@@ -604,17 +614,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes);
-            const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
+            const uint64_t ad = a_hi | (((sA_u32 + stage * Cfg::kABytes) >> 4) & 0x3FFFu);
+            const uint64_t bd = b_hi | (((sB_u32 + stage * Cfg::kBBytes) >> 4) & 0x3FFFu);
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-              const uint64_t ad = operand_desc(a_base, a_mn, kk);
-              const uint64_t bd = operand_desc(b_base, b_mn, kk);
-              const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+              const uint32_t accum = (kk > 0 || kb > kb0) ? 1u : 0u;
               if constexpr (CG == 2)
-                tc_mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+                tc_mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, accum);
               else
-                tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
+                tc_mma_bf16(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, accum);
             }
             if constexpr (CG == 2)
               tc_commit_pair_mc(&empty_bar[stage], static_cast<uint16_t>((1u << CL) - 1u));

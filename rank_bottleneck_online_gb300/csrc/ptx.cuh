@@ -190,6 +190,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return desc;
 }
 
+// The fixed part of a 128-byte-swizzle descriptor (everything but the start address).
+__device__ __forceinline__ uint64_t desc_hi_sw128(uint32_t lbo, uint32_t sbo) {
+  return (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn,
                                                       uint32_t b_mn) {
