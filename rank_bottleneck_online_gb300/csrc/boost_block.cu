@@ -191,7 +191,7 @@ int pick_bn(int64_t n) { return n >= 256 ? 256 : (n >= 128 ? 128 : 64); }
 // arrangement sharing A too when N allows whole 512-wide super-tiles.
 Shape pick_shape(int64_t m, int64_t n, int64_t group, int bn_cap = 256) {
   static const int forced_cg = env_int("BOOST_CG", 0);   // 1 or 2 forces (tuning)
-  static const int mc_limit = env_int("BOOST_MC", 2);    // 1: none, 2: along M, 4: 2 x 2
+  static const int mc_limit = env_int("BOOST_MC", 4);    // 1: none, 2: along M, 4: 2 x 2
   Shape sh{std::min(pick_bn(group > 0 ? group : n), bn_cap), 1, 1, 1};
   if (sh.bn >= 128) sh.cg = (forced_cg == 1 || forced_cg == 2) ? forced_cg : (m >= 256 ? 2 : 1);
   if (sh.cg == 2 && sh.bn == 256 && m >= 512 && mc_limit >= 2) {
