@@ -133,6 +133,23 @@ boost_status boost_block_bwd(const boost_block_desc* desc,
                              void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Backward of the down bottleneck of a LLaMA MLP (no norm) whose input is
+ * h = silu(gate) * up, with the SwiGLU backward fused into the dgrad epilogue: the
+ * block's input gradient dh (rounded to bf16) never reaches HBM; the epilogue reads
+ * gate and up and writes dgate = dh * up * silu'(gate) and dup = dh * silu(gate).
+ * Workload of the technical summary §4 (LLaMA-2 MLP); fusion is this library's.
+ *   h          [T, d]  the block's input (d = the MLP's hidden width)
+ *   A, B, dy   as in boost_block_bwd (desc->has_norm must be 0)
+ *   gate, up   [T, d]  the gate and up projections h was formed from
+ *   dgate, dup [T, d]  out (may be the two halves of one [2, T, d] buffer)
+ *   dA, dB             out, as in boost_block_bwd
+ */
+boost_status boost_block_bwd_swiglu(const boost_block_desc* desc, const void* h, const void* A,
+                                    const void* B, const void* dy, const void* gate,
+                                    const void* up, void* dgate, void* dup, void* dA, void* dB,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Online-RMSNorm statistics alone (technical summary §2.2): per-shard sums of
  * squares and their single combine.
  *   x     [T, d]

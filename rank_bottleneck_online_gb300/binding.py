@@ -31,7 +31,7 @@ EXPORTS = (
     "boost_rmsnorm_stats", "boost_block_layout", "boost_block_check", "boost_status_string",
     "boost_swiglu_fwd", "boost_swiglu_bwd", "boost_add", "boost_debug_wait_timeout",
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
-    "boost_profile_read", "boost_rmsnorm_rstd_noalloc",
+    "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
 )
 
 
@@ -83,6 +83,7 @@ def lib():
     szp = ctypes.POINTER(sz)
     L.boost_block_ws_layout.argtypes = [dp, szp, szp, szp, szp]
     L.boost_rmsnorm_rstd_noalloc.argtypes = [dp, vp, vp, vp]
+    L.boost_block_bwd_swiglu.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_profile_enable.argtypes = [ctypes.c_int]
     L.boost_profile_kernel_count.argtypes = []
     dbl = ctypes.POINTER(ctypes.c_double)
@@ -250,6 +251,32 @@ def block_bwd(desc: Desc, x, gamma, A, B, dy, ws: Workspace, *, rstd=None, dx=No
                                  _ptr(dB), ws.ptr, ws.nbytes, _stream(stream)),
            "boost_block_bwd")
     return dx, dgamma, dA, dB
+
+
+def block_bwd_swiglu(desc: Desc, h, A, B, dy, gate, up, ws: Workspace, *, dgate=None,
+                     dup=None, dA=None, dB=None, stream=None):
+    """Backward of a no-norm block whose input is h = silu(gate)*up: (dgate, dup, dA, dB)."""
+    bf = torch.bfloat16
+    _need(h, "h", bf, (desc.T, desc.d))
+    _need(A, "A", bf, (desc.d, desc.k * desc.r))
+    _need(B, "B", bf, (desc.k, desc.r, desc.n))
+    _need(dy, "dy", bf, (desc.k, desc.T, desc.n))
+    _need(gate, "gate", bf, (desc.T, desc.d))
+    _need(up, "up", bf, (desc.T, desc.d))
+    dev = h.device
+    if dgate is None:
+        dgate = torch.empty(desc.T, desc.d, dtype=bf, device=dev)
+    if dup is None:
+        dup = torch.empty(desc.T, desc.d, dtype=bf, device=dev)
+    if dA is None:
+        dA = torch.empty(desc.d, desc.k * desc.r, dtype=bf, device=dev)
+    if dB is None:
+        dB = torch.empty(desc.k, desc.r, desc.n, dtype=bf, device=dev)
+    _check(lib().boost_block_bwd_swiglu(ctypes.byref(desc), _ptr(h), _ptr(A), _ptr(B), _ptr(dy),
+                                        _ptr(gate), _ptr(up), _ptr(dgate), _ptr(dup), _ptr(dA),
+                                        _ptr(dB), ws.ptr, ws.nbytes, _stream(stream)),
+           "boost_block_bwd_swiglu")
+    return dgate, dup, dA, dB
 
 
 def swiglu_fwd(gate, up, h=None, stream=None):

@@ -54,9 +54,11 @@ class MLP:
     """LLaMA MLP of two bottlenecks: gate/up (normed, k=2) -> SwiGLU -> down (k=1)."""
 
     def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, act="silu", weights=None,
-                 device="cuda", ws=None):
+                 device="cuda", ws=None, fused_glu=True):
         w = weights or {}
         self.T, self.d, self.ffn = T, d, ffn
+        # backward of the down block with the SwiGLU backward in its dgrad epilogue
+        self.fused_glu = fused_glu
         self.gu = Block(T, d, r, 2, ffn, S=S, eps=eps, act=act, has_norm=True,
                         weights={"gamma": w.get("gamma"), "A": w.get("A1"), "B": w.get("B1")},
                         device=device, ws=ws)
@@ -78,8 +80,15 @@ class MLP:
         return self.dn.forward(self.h, stream)[0]
 
     def backward(self, x, dout, stream=None):
-        dh = self.dn.backward(self.h, dout.view(1, self.T, self.d), stream)[0]
-        B.swiglu_bwd(self.gu.y[0], self.gu.y[1], dh, self.dy1[0], self.dy1[1], stream=stream)
+        dy2 = dout.view(1, self.T, self.d)
+        if self.fused_glu:
+            B.block_bwd_swiglu(self.dn.desc, self.h, self.dn.A, self.dn.B, dy2, self.gu.y[0],
+                               self.gu.y[1], self.dn.ws, dgate=self.dy1[0], dup=self.dy1[1],
+                               dA=self.dn.dA, dB=self.dn.dB, stream=stream)
+        else:
+            dh = self.dn.backward(self.h, dy2, stream)[0]
+            B.swiglu_bwd(self.gu.y[0], self.gu.y[1], dh, self.dy1[0], self.dy1[1],
+                         stream=stream)
         return self.gu.backward(x, self.dy1, stream)
 
     def grads(self):

@@ -145,8 +145,8 @@ struct Plan {
   int64_t T, d, r, k, n, kr;
   Shape down, dual, up, dx, wB, wA;
   int tpg_down, tpg_dual;           // super-tiles per group of r columns (K2, K4)
-  int n_cols_dual;                  // BN-wide column tiles of K4 (rows of q partials)
-  int n_cols_wA;                    // BN-wide column tiles of K6 (rows of dgamma partials)
+  int n_cols_dual;                  // rows of K4's q partials (column tiles x halves)
+  int n_cols_wA;                    // rows of K6's dgamma partials (column tiles x halves)
   int splits_B, kbps_B, splits_A, kbps_A;
   size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_part, total;
 };
@@ -210,7 +210,8 @@ Plan make_plan(const boost_block_desc& D, int sms) {
   static const int dual_bn = env_int("BOOST_DUAL_BN", 256);
   P.dual = pick_shape(D.T, P.kr, D.r, dual_bn == 256 ? 256 : (dual_bn == 64 ? 64 : 128));
   P.tpg_dual = static_cast<int>(cdiv(D.r, P.dual.super_n()));
-  P.n_cols_dual = static_cast<int>(P.k * P.tpg_dual * P.dual.mcn);
+  // q partial rows: one per BN-wide column tile per epilogue half
+  P.n_cols_dual = static_cast<int>(P.k * P.tpg_dual * P.dual.mcn * kEpiHalves);
   P.up = pick_shape(D.T, D.n, 0);
   P.dx = pick_shape(D.T, D.d, 0);
   const int64_t nkb_T = cdiv(std::max<int64_t>(D.T, 1), kBK);
@@ -220,7 +221,7 @@ Plan make_plan(const boost_block_desc& D, int sms) {
                 gemm_resident(P.wB.bn, EPI_F32, P.wB.cg, P.wB.mcm, P.wB.mcn, sms),
                 D.k * D.r * D.n, P.splits_B, P.kbps_B);
   P.wA = pick_shape(D.d, P.kr, 0);
-  P.n_cols_wA = static_cast<int>(cdiv(P.kr, P.wA.super_n()) * P.wA.mcn);
+  P.n_cols_wA = static_cast<int>(cdiv(P.kr, P.wA.super_n()) * P.wA.mcn * kEpiHalves);
   const int64_t tiles_A = cdiv(D.d, P.wA.super_m()) * cdiv(P.kr, P.wA.super_n());
   choose_splits(tiles_A, nkb_T,
                 gemm_resident(P.wA.bn, EPI_F32, P.wA.cg, P.wA.mcm, P.wA.mcn, sms),
@@ -459,17 +460,31 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   return cuda_status(e);
 }
 
-boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const void* gamma,
-                             const void* A, const void* B, const float* rstd, const void* dy,
-                             void* dx, void* dgamma, void* dA, void* dB, void* ws,
-                             size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Backward of one block. With `gate` non-NULL the block's input is h = silu(gate) * up
+// (no norm) and, instead of dx, its dgrad epilogue writes dgate and dup.
+boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const void* gamma,
+                            const void* A, const void* B, const float* rstd, const void* dy,
+                            void* dx, void* dgamma, void* dA, void* dB, const void* gate,
+                            const void* up, void* dgate, void* dup, void* ws, size_t ws_bytes,
+                            void* stream) {
   boost_status st = validate_desc(desc);
   if (st != BOOST_OK) return st;
   const boost_block_desc& D = *desc;
+  const bool glu = gate != nullptr;
   if (!D.has_norm && (gamma != nullptr || rstd != nullptr || dgamma != nullptr))
     return BOOST_ERR_INVALID_ARG;
-  st = D.T == 0 ? check_ptrs({A, B, dA, dB}, {gamma, rstd, dgamma, x, dy, dx})
-                : check_ptrs({x, A, B, dy, dx, dA, dB}, {gamma, rstd, dgamma});
+  if (glu) {
+    if (D.has_norm) return BOOST_ERR_INVALID_ARG;
+    st = D.T == 0 ? check_ptrs({A, B, dA, dB}, {x, dy, gate, up, dgate, dup})
+                  : check_ptrs({x, A, B, dy, gate, up, dgate, dup, dA, dB}, {});
+  } else {
+    st = D.T == 0 ? check_ptrs({A, B, dA, dB}, {gamma, rstd, dgamma, x, dy, dx})
+                  : check_ptrs({x, A, B, dy, dx, dA, dB}, {gamma, rstd, dgamma});
+  }
   if (st != BOOST_OK) return st;
   if (D.has_norm && (gamma == nullptr || dgamma == nullptr)) return BOOST_ERR_INVALID_ARG;
   const int sms = current_num_sms();
@@ -639,6 +654,12 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
     w.m_inner = 0;
     w.out = dx;
     w.ldo = P.d;
+    if (glu) {
+      w.out = dgate;
+      w.out2 = dup;
+      w.gate = static_cast<const __nv_bfloat16*>(gate);
+      w.up = static_cast<const __nv_bfloat16*>(up);
+    }
     if (D.has_norm) {
       w.rstd = rs;
       w.qpart = qpart;
@@ -646,12 +667,33 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
       w.d_norm = static_cast<int32_t>(P.d);
       w.xin = static_cast<const __nv_bfloat16*>(x);
     }
-    ProfScope ps(s, K_DX, 2.0 * P.T * P.kr * P.d,
-                 2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (D.has_norm ? 2 : 1)) +
+    ProfScope ps(s, glu ? K_DX_GLU : K_DX, 2.0 * P.T * P.kr * P.d,
+                 2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (glu ? 4 : (D.has_norm ? 2 : 1))) +
                      4.0 * P.T * (P.n_cols_dual + 1));
-    e = launch_gemm(P.dx.bn, EPI_DX, P.dx.cg, P.dx.mcm, P.dx.mcn, w, sms, s);
+    e = launch_gemm(P.dx.bn, glu ? EPI_GLU : EPI_DX, P.dx.cg, P.dx.mcm, P.dx.mcn, w, sms, s);
   }
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const void* gamma,
+                             const void* A, const void* B, const float* rstd, const void* dy,
+                             void* dx, void* dgamma, void* dA, void* dB, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return block_bwd_impl(desc, x, gamma, A, B, rstd, dy, dx, dgamma, dA, dB, nullptr, nullptr,
+                        nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+boost_status boost_block_bwd_swiglu(const boost_block_desc* desc, const void* h, const void* A,
+                                    const void* B, const void* dy, const void* gate,
+                                    const void* up, void* dgate, void* dup, void* dA, void* dB,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  if (gate == nullptr) return BOOST_ERR_INVALID_ARG;
+  return block_bwd_impl(desc, h, nullptr, A, B, nullptr, dy, nullptr, nullptr, dA, dB, gate, up,
+                        dgate, dup, ws, ws_bytes, stream);
 }
 
 boost_status boost_block_ws_layout(const boost_block_desc* desc, size_t* off_a, size_t* off_dzs,

@@ -7,8 +7,9 @@
 //   warp 1         : allocates TMEM; lane 0 (of the even CTA when CG = 2) issues
 //                    tcgen05.mma (M=128*CG, N=BN, K=16) into a TMEM accumulator and
 //                    commits the stage / accumulator barriers
-//   warps 2..5     : epilogue; tcgen05.ld of the accumulator (one TMEM lane quarter
-//                    per warp, one output row per thread), fused math, global stores
+//   warps 2..9     : epilogue; tcgen05.ld of the accumulator (two warps per TMEM lane
+//                    quarter taking alternate 32-column chunks, one output row per
+//                    thread), fused math, global stores
 // CG = 2 runs each tile on a CTA pair (a cluster of two SMs, tcgen05 cta_group::2):
 // each SM stages its own 128 rows of A and half of the BN rows of B, so the operand
 // bytes each SM moves per MMA flop are 2/3 of the single-SM tile's. The even CTA
@@ -40,7 +41,9 @@ namespace boost_gb300 {
 constexpr int kBM = 128;           // rows per tile (TMEM lanes)
 constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
-constexpr int kNumThreads = 192;   // 6 warps
+constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, alternating 32-column chunks
+constexpr int kEpiHalves = kEpiWarps / 4;
+constexpr int kNumThreads = 32 * (2 + kEpiWarps);   // producer, MMA issuer, epilogue
 
 enum EpiMode : int {
   EPI_ACT = 0,     // out_bf16 = act(s_row * acc)               (down-projection fwd)
@@ -49,6 +52,7 @@ enum EpiMode : int {
   EPI_DUAL = 3,    // two accumulators: a, dzs, per-row q partials (recompute + dgrad)
   EPI_DX = 4,      // out_bf16 = acc - (s^2 q / d) x            (dgrad x + RMSNorm bwd)
   EPI_DA = 5,      // out_bf16 = gamma_row * acc, dgamma partials (wgrad of A)
+  EPI_GLU = 6,     // dh = bf16(acc); out = dh*up*silu'(gate), out2 = dh*silu(gate) (SwiGLU bwd)
 };
 
 struct OperandView {
@@ -93,6 +97,8 @@ struct GemmParams {
   const __nv_bfloat16* xin;   // EPI_DX: x [M, N]
   const __nv_bfloat16* gamma; // EPI_DA: gamma [M]
   const __nv_bfloat16* wA;    // EPI_DA: A [M, N]
+  const __nv_bfloat16* gate;  // EPI_GLU: gate [M, N]
+  const __nv_bfloat16* up;    // EPI_GLU: up [M, N]
   DeviceError* err;
   uint64_t wait_limit_ns;
 };
@@ -112,7 +118,7 @@ struct GemmCfg {
   static constexpr int kTmemCols = kTmemColsRaw <= 32 ? 32 : kTmemColsRaw <= 64 ? 64
                                    : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAccStages + 1) + 16;
-  static constexpr int kStgBytes = 4 * 4096;                      // epilogue staging, 4 KB per warp
+  static constexpr int kStgBytes = kEpiWarps * 4096;              // epilogue staging, 4 KB per warp
   static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 127) / 128 * 128;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStgOffset + kStgBytes;
   static constexpr int kMmaM = kBM * CG;                    // M of one tcgen05.mma
@@ -128,6 +134,7 @@ struct GemmCfg {
   static_assert(kMmaM == 128 || kMmaM == 256, "tcgen05.mma kind::f16 M is 128 or 256 here");
   static_assert(kBRows % 64 == 0, "each CTA stages whole 64-row B boxes");
   static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit per CTA");
 };
 
 struct TileCoord {
@@ -285,6 +292,42 @@ __device__ __forceinline__ void stage_store_f32(uint8_t* stg, int lane, const fl
   __syncwarp();
 }
 
+// Two halves of a coalesced 32 x 32 bf16 block read, so a caller can start the global
+// loads of the next block before finishing the current one: issue reads this lane's
+// four 16-byte pieces (rows 8j + lane/4, chunk lane%4) into registers; finish passes
+// them through the staging block and returns this lane's row in fp32.
+__device__ __forceinline__ void stage_issue_bf16(int lane, const __nv_bfloat16* g, int64_t ld,
+                                                 int rows_valid, int cols_valid, uint4 (&q)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2), c = lane & 3;
+    q[j] = make_uint4(0, 0, 0, 0);
+    if (r < rows_valid && c * 8 < cols_valid)
+      q[j] = *reinterpret_cast<const uint4*>(g + static_cast<int64_t>(r) * ld + c * 8);
+  }
+}
+
+__device__ __forceinline__ void stage_finish_bf16(uint8_t* stg, int lane, const uint4 (&q)[4],
+                                                  float (&out)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2), c = lane & 3;
+    reinterpret_cast<uint4*>(stg + r * 64)[c ^ ((r >> 1) & 3)] = q[j];
+  }
+  __syncwarp();
+  const uint4* mine = reinterpret_cast<const uint4*>(stg + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = mine[c ^ sw];
+    out[8 * c + 0] = bf16_lo(u.x); out[8 * c + 1] = bf16_hi(u.x);
+    out[8 * c + 2] = bf16_lo(u.y); out[8 * c + 3] = bf16_hi(u.y);
+    out[8 * c + 4] = bf16_lo(u.z); out[8 * c + 5] = bf16_hi(u.z);
+    out[8 * c + 6] = bf16_lo(u.w); out[8 * c + 7] = bf16_hi(u.w);
+  }
+  __syncwarp();
+}
+
 // Coalesced read of a 32 x 32 bf16 block (row r at g + r*ld), delivered as this lane's
 // row in fp32; out-of-range rows or columns read as zero.
 __device__ __forceinline__ void stage_load_bf16(uint8_t* stg, int lane, const __nv_bfloat16* g,
@@ -316,11 +359,13 @@ __device__ __forceinline__ void stage_load_bf16(uint8_t* stg, int lane, const __
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
 // `col_tile` indexes the per-row partial sums (q, dgamma) of this BN-wide column tile.
+// `half` selects the 32-column chunks of this warp (half, half + kEpiHalves, ...); the
+// per-row partial sums are written per half, at row col_tile * kEpiHalves + half.
 template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
                                               int32_t row0, int32_t n0, int32_t n_end,
                                               uint32_t t_row, uint8_t* stg, int lane,
-                                              int32_t col_tile) {
+                                              int32_t col_tile, int half) {
   const int32_t row = row0 + lane;
   const bool row_ok = row < p.M;
   const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
@@ -341,8 +386,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   if constexpr (MODE == EPI_DA) {
     if (p.gamma != nullptr && row_ok) g_row = __bfloat162float(p.gamma[row]);
   }
+  uint4 gq[4], uq[4];   // EPI_GLU: gate / up pieces of the next 32-column chunk, in flight
+  if constexpr (MODE == EPI_GLU) {
+    const int32_t c0 = n0 + half * 32;
+    stage_issue_bf16(lane, p.gate + static_cast<int64_t>(row0) * p.ldo + c0, p.ldo, rows_valid,
+                     n_end - c0, gq);
+    stage_issue_bf16(lane, p.up + static_cast<int64_t>(row0) * p.ldo + c0, p.ldo, rows_valid,
+                     n_end - c0, uq);
+  }
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = half; c < BN / 32; c += kEpiHalves) {
     const int32_t col0 = n0 + c * 32;
     const int cols_valid = n_end - col0;
     if (cols_valid <= 0) break;            // warp-uniform: the rest of the tile is outside N
@@ -392,6 +445,37 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
                             static_cast<int64_t>(row0) * p.ldo + col0;
         stage_store_bf16(stg, lane, pk2, o2, p.ldo, rows_valid, cols_valid);
+      } else if constexpr (MODE == EPI_GLU) {
+        // SwiGLU backward on the down-projection's input gradient dh (rounded to bf16,
+        // the value a separate pass would have stored): dgate and dup of h = silu(g)*u.
+        float gv[32], uv[32];
+        stage_finish_bf16(stg, lane, gq, gv);
+        stage_finish_bf16(stg, lane, uq, uv);
+        const int32_t nxt = col0 + 32 * kEpiHalves;   // this warp's next chunk
+        if (c + kEpiHalves < BN / 32 && nxt < n_end) {   // warp-uniform: prefetch it
+          stage_issue_bf16(lane, p.gate + static_cast<int64_t>(row0) * p.ldo + nxt, p.ldo,
+                           rows_valid, n_end - nxt, gq);
+          stage_issue_bf16(lane, p.up + static_cast<int64_t>(row0) * p.ldo + nxt, p.ldo,
+                           rows_valid, n_end - nxt, uq);
+        }
+        uint32_t pk2[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float dgo[2], duo[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float dh = __bfloat162float(__float2bfloat16_rn(v[i + h]));
+            const float z = gv[i + h];
+            const float sg = sigmoid_f(z);
+            dgo[h] = dh * uv[i + h] * (sg * (1.0f + z * (1.0f - sg)));
+            duo[h] = dh * (z * sg);
+          }
+          pk[i / 2] = pack_bf16x2(dgo[0], dgo[1]);
+          pk2[i / 2] = pack_bf16x2(duo[0], duo[1]);
+        }
+        __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
+                            static_cast<int64_t>(row0) * p.ldo + col0;
+        stage_store_bf16(stg, lane, pk2, o2, p.ldo, rows_valid, cols_valid);
       } else if constexpr (MODE == EPI_DX) {
         float xv[32];
         if (__any_sync(0xffffffffu, coef != 0.0f)) {   // warp-uniform: the load is cooperative
@@ -423,11 +507,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
   if constexpr (MODE == EPI_DUAL) {
     if (row_ok && p.qpart != nullptr)
-      p.qpart[static_cast<int64_t>(col_tile) * p.M + row] = rowsum;
+      p.qpart[static_cast<int64_t>(col_tile * kEpiHalves + half) * p.M + row] = rowsum;
   }
   if constexpr (MODE == EPI_DA) {
     if (row_ok && p.dgpart != nullptr)
-      p.dgpart[static_cast<int64_t>(col_tile) * p.M + row] = rowsum;
+      p.dgpart[static_cast<int64_t>(col_tile * kEpiHalves + half) * p.M + row] = rowsum;
   }
 }
 
@@ -468,7 +552,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     for (int s = 0; s < Cfg::kAccStages; ++s) {
       mbar_init(&tfull_bar[s], 1);
-      mbar_init(&tempty_bar[s], 4 * CG);    // one arrival per epilogue warp of the pair
+      mbar_init(&tempty_bar[s], kEpiWarps * CG);   // one arrival per epilogue warp of the pair
     }
     mbar_init(done_bar, 1);
     fence_barrier_init();
@@ -656,6 +740,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                    // TMEM lane quarter of this warp
+    const int half = (warp - 2) / 4;           // which alternate column chunks it takes
     uint8_t* stg = smem + Cfg::kStgOffset + (warp - 2) * 4096;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -671,7 +756,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int32_t pn0 = tc.n0 + static_cast<int32_t>(pn) * BN;
       const int32_t pend = min(pn0 + BN, tc.n_end);
       epilogue_tile<BN, MODE>(p, tc, row0, pn0, pend, t_row, stg, lane,
-                              tc.n_blk * MCN + static_cast<int32_t>(pn));
+                              tc.n_blk * MCN + static_cast<int32_t>(pn), half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

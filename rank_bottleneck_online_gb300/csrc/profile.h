@@ -23,6 +23,7 @@ enum KernelId : int {
   K_SWIGLU_BWD,
   K_ADD,
   K_PROBE,
+  K_DX_GLU,
   K_COUNT
 };
 

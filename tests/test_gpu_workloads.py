@@ -46,6 +46,24 @@ def test_mlp_parity(T, d, r, ffn, S):
         assert_close(k, v, g[k])
 
 
+@pytest.mark.parametrize("T,d,r,ffn", [(512, 256, 128, 512), (600, 128, 64, 520)])
+def test_fused_swiglu_backward_matches_separate_passes(T, d, r, ffn):
+    # the down block's dgrad epilogue computing dgate/dup equals dx + a SwiGLU pass
+    w = inputs.make_mlp(T, d, r, ffn, seed=6)
+    x, dout = w["x"].cuda(), w["dout"].cuda()
+    res = []
+    for fused in (True, False):
+        mlp = MLP(T, d, r, ffn, S=2, weights=w, fused_glu=fused)
+        mlp.forward(x)
+        mlp.backward(x, dout)
+        B.check(mlp.gu.ws)
+        res.append((mlp.dy1.clone(), {k: v.clone() for k, v in mlp.grads().items()}))
+    (dy_f, g_f), (dy_s, g_s) = res
+    assert_close("dgate/dup", dy_f, dy_s.double().cpu().numpy(), 1e-2, 1e-3)
+    for k in g_f:
+        assert_close(k, g_f[k], g_s[k].double().cpu().numpy(), 1e-2, 1e-3)
+
+
 def test_layer_parity():
     T, d, r, ffn, S = 256, 256, 64, 384, 4
     w = inputs.make_layer(T, d, r, ffn, seed=2)
