@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 METRIC = "bottleneck-block fwd+bwd TFLOP/s & tokens/s on 1 GB300; % of roofline"
 WORKLOAD = "llama2_7b_mlp"
 CPU_SAMPLE_T = 1024          # tokens of the CPU-baseline sample (full d, r, ffn)
-REF_SAMPLE_T = 256           # tokens per step of the reference arm
+REF_STEP_T = 16              # tokens per step of the reference arm
 
 
 def mlp_flops(T, d, r, ffn):
@@ -159,17 +159,24 @@ def _oracle_sample_main(T_sample, steps):
 
 
 def reference_arm(args, rank, world):
-    """The oracle, as it stands, on the host cores: rank 0 only."""
+    """The oracle, as it stands, on the host cores: rank 0 only.
+
+    A step is REF_STEP_T tokens of the workload (full widths). The K timed steps'
+    token samples are independent rows, so they are processed in one oracle pass of
+    K * REF_STEP_T tokens (the oracle's per-call cost of rounding the weights would
+    otherwise dominate); likewise the warm-up steps, untimed, before it.
+    """
     if rank != 0:
         return 0
     c = _cfg()
-    T_s = REF_SAMPLE_T
-    res = cpu_oracle_sample(T_s, steps=args.warmup + args.steps)
-    secs = res["seconds"][args.warmup:]
-    per = sum(secs) / len(secs)
+    cpu_oracle_sample(args.warmup * REF_STEP_T, steps=1)
+    res = cpu_oracle_sample(args.steps * REF_STEP_T, steps=1)
+    per = res["seconds"][0] / args.steps
+    T_s = REF_STEP_T
     value = T_s / per
     exe, _ = mlp_flops(T_s, c["d"], c["r"], c["ffn"])
-    sample = (f"{T_s} of {c['T']} tokens of {WORKLOAD} per step (full d/r/ffn), oracle bf16 "
+    sample = (f"{T_s} of {c['T']} tokens of {WORKLOAD} per step (full d/r/ffn), the "
+              f"{args.steps} timed steps in one pass of {args.steps * T_s} tokens; oracle bf16 "
               "flow fwd+bwd in numpy fp64")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -184,6 +191,23 @@ def reference_arm(args, rank, world):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ------------------------------------------------------------- ranks
+
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The maximum of a per-rank float over all ranks (identity on one process)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world, units_per_rank, seconds):
+    """Whole-job rate under weak scaling: every rank processes the same units."""
+    return world * units_per_rank / seconds
 
 
 # ------------------------------------------------------------- ours
@@ -271,11 +295,7 @@ def ours_arm(args, rank, world, local_rank):
     prof = B.profile_read()
     B.profile_enable(False)
     B.check(mlp.gu.ws)
-    ms_total = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     e2e_s = float("nan") if args.skip_aux else _e2e(args, mlp, w, x, dout, T, d, barrier,
                                                     dist, dev)
@@ -312,17 +332,12 @@ def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
     for _ in range(args.steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    return e2e_s
+    return max_over_ranks(time.perf_counter() - t0, dist, dev)
 
 
 def _report(args, world, prof, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn, S):
     ms_step = ms_total / args.steps
-    tokens_per_s = world * T * args.steps / (ms_total / 1e3)
+    tokens_per_s = aggregate_rate(world, T * args.steps, ms_total / 1e3)
     exe, model = mlp_flops(T, d, r, ffn)
     tflops = world * exe * args.steps / (ms_total / 1e3) / 1e12
     peaks = load_peaks()
@@ -384,7 +399,7 @@ def _report(args, world, prof, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn, S)
         "kernels": kernels,
         "gpu_launches": gpu_launches,
         "e2e": None if args.skip_aux else {
-            "value": world * T * args.steps / e2e_s, "unit": "tokens/s",
+            "value": aggregate_rate(world, T * args.steps, e2e_s), "unit": "tokens/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "clocks": clocks,
         "cpu_baseline": cpu,

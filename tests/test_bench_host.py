@@ -1,0 +1,62 @@
+"""Host-side checks of bench.py: the multi-rank timing reduction over gloo ranks on
+CPU (world size 2), the weak-scaling aggregate, the FLOP model, and the reference
+arm's rank handling. No GPU is used."""
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = 10.0 + 5.0 * rank           # each rank's own elapsed time
+        dist.barrier()
+        m = bench.max_over_ranks(local, dist, "cpu")
+        out[rank] = m
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    port = _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1] == 15.0
+
+
+def test_single_process_max_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_weak_scaling_aggregate():
+    # N replicas each processing T*K tokens in the slowest rank's time
+    assert bench.aggregate_rate(4, 16384 * 10, 2.0) == 4 * 16384 * 10 / 2.0
+
+
+def test_flop_model_matches_per_block_formula():
+    exe, model = bench.mlp_flops(16384, 4096, 1024, 11008)
+    assert exe == 5205500362752          # 8 T d kr + 6 T kr n per block, two blocks
+    assert model == (6 * 16384 * 4096 * 2048 + 6 * 16384 * 2048 * 11008 +
+                     6 * 16384 * 11008 * 1024 + 6 * 16384 * 1024 * 4096)
+
+
+def test_reference_arm_nonzero_ranks_do_no_work(capsys):
+    class A:
+        steps, warmup = 1, 0
+    assert bench.reference_arm(A(), rank=1, world=2) == 0
+    assert capsys.readouterr().out == ""

@@ -4,6 +4,7 @@ core, the SVD-style pair, and the full-size LLaMA-2-1B attention-projection
 block.
 """
 
+import numpy as np
 import pytest
 import torch
 
@@ -120,3 +121,85 @@ def test_llama2_1b_attention_block_full_size():
     assert_close("y", blk.y, y)
     for key, got in (("dx", blk.dx), ("dA", blk.dA), ("dB", blk.dB), ("dgamma", blk.dgamma)):
         assert_close(key, got, g[key])
+
+
+# ------------------------------------------------ full-size configurations
+
+@pytest.mark.slow
+def test_llama2_7b_mlp_full_size():
+    """The benchmarked workload at full size, every output against the full oracle."""
+    c = inputs.CONFIGS["llama2_7b_mlp"]
+    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
+    w = inputs.make_mlp(T, d, r, ffn, seed=0)
+    mlp = MLP(T, d, r, ffn, S=S, weights=w)
+    x, dout = w["x"].cuda(), w["dout"].cuda()
+    out = mlp.forward(x).clone()
+    mlp.backward(x, dout)
+    B.check(mlp.gu.ws)
+    got = {k: v.cpu() for k, v in mlp.grads().items()}
+    out = out.cpu()
+    del mlp
+    torch.cuda.empty_cache()
+    args = f64(w, ("x", "gamma", "A1", "B1", "A2", "B2"))
+    o, _ = oracle.mlp_fwd(*args, S=S)
+    assert_close("out", out, o)
+    del o
+    g = oracle.mlp_bwd(*args, inputs.as_f64(w["dout"]), S=S)
+    for k, v in got.items():
+        assert_close(k, v, g[k])
+
+
+def _sample_rows(T, n=192, seed=0):
+    # spread over every 256-row tile pair, plus the first and last rows
+    rng = np.random.default_rng(seed)
+    idx = np.unique(np.concatenate([[0, T - 1], rng.choice(T, n, replace=False)]))
+    return np.sort(idx)
+
+
+@pytest.mark.slow
+def test_llama2_13b_layer_full_size_sampled_rows():
+    """Full-size layer on the GPU; output and dx rows checked against the oracle run
+    on those rows alone (every step of the layer is row-wise)."""
+    c = inputs.CONFIGS["llama2_13b_layer"]
+    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
+    w = inputs.make_layer(T, d, r, ffn, seed=0)
+    layer = Layer(T, d, r, ffn, S=S, weights=w["p"])
+    x = w["x"].cuda()
+    out = layer.forward(x).clone()
+    layer.backward(x, w["dout"].cuda(), w["dq"].cuda(), w["dk"].cuda())
+    B.check(layer.qkv.ws)
+    idx = _sample_rows(T)
+    out_s, dx_s = out.cpu()[idx], layer.dx.cpu()[idx]
+    del layer
+    torch.cuda.empty_cache()
+    p = {k: inputs.as_f64(v) for k, v in w["p"].items()}
+    xs = inputs.as_f64(w["x"])[idx]
+    o, _ = oracle.layer_fwd(xs, p, S=S)
+    assert_close("out rows", out_s, o)
+    g = oracle.layer_bwd(xs, p, *(inputs.as_f64(w[k])[idx] for k in ("dout", "dq", "dk")), S=S)
+    assert_close("dx rows", dx_s, g["dx"])
+
+
+@pytest.mark.slow
+def test_svd_40b_pair_full_size_sampled_rows():
+    c = inputs.CONFIGS["svd_40b_pair"]
+    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
+    w = inputs.make_svd_pair(T, d, r, ffn, seed=0)
+    pair = SVDPair(T, d, r, ffn, S=S, weights=w["p"])
+    x = w["x"].cuda()
+    yq, yg = pair.forward(x)
+    yq, yg = yq.clone(), yg.clone()
+    pair.backward(x, w["dy_qkv"].cuda(), w["dy_gu"].cuda())
+    B.check(pair.qkv.ws)
+    idx = _sample_rows(T)
+    yq_s, yg_s, dx_s = yq.cpu()[:, idx], yg.cpu()[:, idx], pair.dx.cpu()[idx]
+    del pair
+    torch.cuda.empty_cache()
+    p = {k: inputs.as_f64(v) for k, v in w["p"].items()}
+    xs = inputs.as_f64(w["x"])[idx]
+    oq, og = oracle.svd_pair_fwd(xs, p, S=S)
+    assert_close("y_qkv rows", yq_s, oq)
+    assert_close("y_gu rows", yg_s, og)
+    g = oracle.svd_pair_bwd(xs, p, inputs.as_f64(w["dy_qkv"])[:, idx],
+                            inputs.as_f64(w["dy_gu"])[:, idx], S=S)
+    assert_close("dx rows", dx_s, g["dx"])
