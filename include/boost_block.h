@@ -248,13 +248,19 @@ boost_status boost_debug_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_
  *   boost_profile_kernel_count() is the number of kernel ids.
  *   boost_profile_read(id, ...) synchronises the pending events and returns the
  *   kernel's static name, launch count, summed event time in milliseconds and
- *   summed algorithmic flops and bytes. Any output pointer may be NULL.
+ *   summed algorithmic flops and bytes. Any output pointer may be NULL. A
+ *   "launch" here is one timed operation: a GEMM whose rows are split over two
+ *   concurrent kernels (the co-scheduled launch shape) counts once, its time
+ *   spanning both.
+ *   boost_profile_read_kernels(id, &kernels) returns the number of kernels those
+ *   operations launched (>= the launch count). kernels must not be NULL.
  * Process-wide; intended for one measuring thread.
  */
 boost_status boost_profile_enable(int on);
 int boost_profile_kernel_count(void);
 boost_status boost_profile_read(int id, const char** name, int64_t* launches, double* total_ms,
                                 double* total_flops, double* total_bytes);
+boost_status boost_profile_read_kernels(int id, int64_t* kernels);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,7 @@ EXPORTS = (
     "boost_swiglu_fwd", "boost_swiglu_bwd", "boost_add", "boost_debug_wait_timeout",
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
+    "boost_profile_read_kernels",
 )
 
 
@@ -89,6 +90,7 @@ def lib():
     dbl = ctypes.POINTER(ctypes.c_double)
     L.boost_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                                      ctypes.POINTER(i64), dbl, dbl, dbl]
+    L.boost_profile_read_kernels.argtypes = [ctypes.c_int, ctypes.POINTER(i64)]
     for name in EXPORTS:
         if name != "boost_block_workspace_bytes" and name != "boost_status_string":
             getattr(L, name).restype = ctypes.c_int
@@ -323,6 +325,22 @@ def check(ws: Workspace, stream=None):
 
 def profile_enable(on: bool):
     _check(lib().boost_profile_enable(1 if on else 0), "boost_profile_enable")
+
+
+def profile_kernels():
+    """{kernel name: kernels launched} for kernels that ran (an operation split over
+    concurrent launches counts each of them)."""
+    L = lib()
+    out = {}
+    for i in range(L.boost_profile_kernel_count()):
+        name = ctypes.c_char_p()
+        n = ctypes.c_int64(0)
+        _check(L.boost_profile_read(i, ctypes.byref(name), None, None, None, None),
+               "boost_profile_read")
+        _check(L.boost_profile_read_kernels(i, ctypes.byref(n)), "boost_profile_read_kernels")
+        if n.value:
+            out[name.value.decode()] = n.value
+    return out
 
 
 def profile_read():

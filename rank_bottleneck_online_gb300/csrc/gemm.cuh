@@ -78,6 +78,8 @@ struct GemmParams {
   int32_t M, N;               // output extent (per batch)
   int32_t batch;              // batches in the tile list
   int32_t m_tiles, n_tiles;
+  int32_t m_base;             // first output row of this launch (rows [m_base, m_base+m_extent))
+  int32_t m_extent;           // rows of this launch (0: all of M from m_base)
   int32_t splits, kb_per_split;
   int32_t m_inner;            // tile order: 1 = m fastest within (batch, split)
   int32_t group_n;            // columns per group (grouped tiling)
@@ -161,7 +163,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int32_t ti
   TileCoord c;
   c.split = bs / p.batch;
   c.batch = bs - c.split * p.batch;
-  c.m0 = mb * TILE_M;
+  c.m0 = p.m_base + mb * TILE_M;
   c.n_blk = nb;
   if (p.group_tiles > 0) {
     c.group = nb / p.group_tiles;
@@ -189,9 +191,11 @@ __device__ __forceinline__ void kb_range(const GemmParams& p, int seg, int32_t s
   }
 }
 
-// Issue the TMA boxes of one operand tile (`rows` MN rows x 64 K) into `dst`.
-// CG = 1 completes on the local barrier `bar`; CG = 2 on the pair barrier at cluster
-// address `bar_cluster` (the even CTA's stage barrier).
+// Issue the TMA boxes of one operand tile (`rows` MN rows x 64 K) into `dst`: every box
+// covers 64 MN rows x 64 K (K-major: 64 rows of 128 B; MN-major: one 64-wide atom of
+// 64 K rows), 8 KB, placed at dst + 8 KB * j. One set of tensor maps therefore serves
+// every tile shape. CG = 1 completes on the local barrier `bar`; CG = 2 on the pair
+// barrier at cluster address `bar_cluster` (the even CTA's stage barrier).
 template <int CG>
 __device__ __forceinline__ void load_operand(const CUtensorMap* tm, const OperandView& v,
                                              uint8_t* dst, uint64_t* bar, uint32_t bar_cluster,
@@ -199,20 +203,12 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* tm, const Operan
   int32_t c[3] = {0, 0, 0};
   c[v.k_dim] = k;
   c[v.b_dim] = b;
-  if (v.mn_major) {
-    for (int j = 0; j < rows / 64; ++j) {
-      c[v.mn_dim] = mn + 64 * j;
-      if constexpr (CG == 2)
-        tma_load_3d_pair(dst + j * 8192, tm, bar_cluster, c[0], c[1], c[2]);
-      else
-        tma_load_3d(dst + j * 8192, tm, bar, c[0], c[1], c[2]);
-    }
-  } else {
-    c[v.mn_dim] = mn;
+  for (int j = 0; j < rows / 64; ++j) {
+    c[v.mn_dim] = mn + 64 * j;
     if constexpr (CG == 2)
-      tma_load_3d_pair(dst, tm, bar_cluster, c[0], c[1], c[2]);
+      tma_load_3d_pair(dst + j * 8192, tm, bar_cluster, c[0], c[1], c[2]);
     else
-      tma_load_3d(dst, tm, bar, c[0], c[1], c[2]);
+      tma_load_3d(dst + j * 8192, tm, bar, c[0], c[1], c[2]);
   }
 }
 

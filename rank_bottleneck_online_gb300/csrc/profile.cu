@@ -24,10 +24,11 @@ struct Pending {
   int id;
   cudaEvent_t e0, e1;
   double flops, bytes;
+  int kernels;
 };
 
 struct Totals {
-  int64_t launches = 0;
+  int64_t launches = 0, kernels = 0;
   double ms = 0.0, flops = 0.0, bytes = 0.0;
 };
 
@@ -36,6 +37,7 @@ std::mutex g_mu;
 std::vector<Pending> g_pending;
 std::vector<cudaEvent_t> g_pool;
 Totals g_tot[K_COUNT];
+thread_local ProfScope* t_open = nullptr;
 
 cudaEvent_t take_event() {
   if (!g_pool.empty()) {
@@ -58,6 +60,7 @@ void drain_locked() {
         cudaEventElapsedTime(&ms, p.e0, p.e1) == cudaSuccess) {
       Totals& t = g_tot[p.id];
       t.launches += 1;
+      t.kernels += p.kernels;
       t.ms += ms;
       t.flops += p.flops;
       t.bytes += p.bytes;
@@ -81,14 +84,21 @@ ProfScope::ProfScope(cudaStream_t s, int id, double flops, double bytes)
   if (e0_ && e1_) {
     cudaEventRecord(e0_, stream_);
     active_ = true;
+    outer_ = t_open;
+    t_open = this;
   }
 }
 
 ProfScope::~ProfScope() {
   if (!active_) return;
+  t_open = outer_;
   std::lock_guard<std::mutex> lk(g_mu);
   cudaEventRecord(e1_, stream_);
-  g_pending.push_back(Pending{id_, e0_, e1_, flops_, bytes_});
+  g_pending.push_back(Pending{id_, e0_, e1_, flops_, bytes_, kernels_});
+}
+
+void prof_note_kernels(int extra) {
+  if (t_open != nullptr) t_open->kernels_ += extra;
 }
 
 }  // namespace boost_gb300
@@ -108,6 +118,14 @@ boost_status boost_profile_enable(int on) {
 }
 
 int boost_profile_kernel_count(void) { return K_COUNT; }
+
+boost_status boost_profile_read_kernels(int id, int64_t* kernels) {
+  if (id < 0 || id >= K_COUNT || kernels == nullptr) return BOOST_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  drain_locked();
+  *kernels = g_tot[id].kernels;
+  return BOOST_OK;
+}
 
 boost_status boost_profile_read(int id, const char** name, int64_t* launches, double* total_ms,
                                 double* total_flops, double* total_bytes) {

@@ -27,8 +27,9 @@ enum KernelId : int {
   K_COUNT
 };
 
-// Brackets one launch with events on `s` when profiling is enabled; `flops` and
-// `bytes` are the launch's algorithmic work.
+// Brackets one operation with events on `s` when profiling is enabled; `flops` and
+// `bytes` are the operation's algorithmic work. An operation is one kernel launch
+// unless the code inside the scope reports more with prof_note_kernels.
 class ProfScope {
  public:
   ProfScope(cudaStream_t s, int id, double flops, double bytes);
@@ -42,6 +43,13 @@ class ProfScope {
   double flops_, bytes_;
   cudaEvent_t e0_ = nullptr, e1_ = nullptr;
   bool active_ = false;
+  int kernels_ = 1;
+  ProfScope* outer_ = nullptr;
+  friend void prof_note_kernels(int extra);
 };
+
+// Adds `extra` kernel launches to the innermost open scope of this thread (an
+// operation split over several concurrent launches).
+void prof_note_kernels(int extra);
 
 }  // namespace boost_gb300

@@ -7,6 +7,8 @@ accumulator recompute/dgrad, both weight gradients (split-K and not) and dx
 with the RMSNorm backward, on shapes that span several tiles and ragged tails.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -57,6 +59,9 @@ CASES = [
     ("identity_act", 256, 320, 128, 3, 384, 8, "identity", True),
     ("many_tiles", 1000, 512, 128, 2, 1000, 4, "silu", True),
     ("single_row", 1, 64, 64, 1, 64, 2, "silu", True),
+    # >= 8 row super-tiles of 2 x 2 clusters: the row GEMMs split their last rows
+    # into a concurrent CTA-pair launch; T is not a multiple of either launch's tile
+    ("co_scheduled_rows", 4352, 512, 512, 2, 1024, 4, "silu", True),
 ]
 
 
@@ -95,6 +100,31 @@ def test_recompute_is_bitwise_equal_to_forward(case):
     # the backward regenerates a from x inside the block; it must be the forward's a
     _, _, a_fwd, a_bwd = _run_block(*case)
     assert torch.equal(a_fwd, a_bwd)
+
+
+@pytest.mark.skipif(os.environ.get("BOOST_COSCHED", "") == "0",
+                    reason="co-scheduling turned off in the environment")
+def test_co_scheduled_gemms_count_two_kernels():
+    # T = 4352 rows take the split launch shape for every GEMM over the token rows;
+    # the profiler counts one timed operation and two kernels for each of them
+    T, d, r, k, n, S = 4352, 512, 512, 2, 1024, 4
+    w = inputs.make_block(T, d, r, k, n, seed=6)
+    blk = Block(T, d, r, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    B.profile_enable(True)
+    try:
+        blk.forward(x)
+        blk.backward(x, dy)
+        torch.cuda.synchronize()
+        ops = B.profile_read()
+        kernels = B.profile_kernels()
+    finally:
+        B.profile_enable(False)
+    for name in ("gemm_down_act", "gemm_up", "gemm_dual", "gemm_dx"):
+        assert ops[name][0] == 1, name
+        assert kernels[name] == 2, name
+    for name in ("gemm_wgrad_A", "gemm_wgrad_B", "rmsnorm_stats"):
+        assert kernels[name] == ops[name][0], name
 
 
 def test_backward_with_and_without_saved_rstd_agree():
