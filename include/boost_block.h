@@ -109,6 +109,24 @@ boost_status boost_block_fwd(const boost_block_desc* desc,
                              void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Forward of the gate/up bottleneck of a LLaMA MLP (k == 2: group 0 = gate,
+ * group 1 = up) with the SwiGLU forward fused into the up-projection: one
+ * tensor-core kernel accumulates the gate and the up group of an output tile in
+ * two TMEM accumulators and its epilogue writes gate = y[0] and up = y[1] (the
+ * backward needs them) and h = silu(gate) * up, formed from the bf16 gate and up
+ * values, so no separate pass reads gate and up back. Workload of the technical
+ * summary §4 (LLaMA-2 MLP); the fusion is this library's.
+ *   x, gamma, A, B, rstd, ws  as in boost_block_fwd; desc->k must be 2
+ *   y      [2, T, n]  out: gate and up
+ *   h      [T, n]     out: silu(gate) * up (may be NULL only when T == 0)
+ * Errors: as boost_block_fwd, plus BOOST_ERR_INVALID_ARG for k != 2 or a NULL h.
+ */
+boost_status boost_block_fwd_swiglu(const boost_block_desc* desc,
+                                    const void* x, const void* gamma, const void* A,
+                                    const void* B, void* y, void* h, float* rstd,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Backward of one block with recompute (technical summary §2.2,
  * communication-free low-rank activation checkpointing: only x is kept; the
  * r-wide activation is regenerated inside the block).

@@ -32,7 +32,7 @@ EXPORTS = (
     "boost_swiglu_fwd", "boost_swiglu_bwd", "boost_add", "boost_debug_wait_timeout",
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
-    "boost_profile_read_kernels",
+    "boost_profile_read_kernels", "boost_block_fwd_swiglu",
 )
 
 
@@ -70,6 +70,7 @@ def lib():
     L.boost_block_workspace_bytes.restype = sz
     L.boost_block_ws_init.argtypes = [vp, sz, vp]
     L.boost_block_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.boost_block_fwd_swiglu.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_rmsnorm_stats.argtypes = [dp, vp, vp, vp, vp]
     L.boost_block_layout.argtypes = [dp, ctypes.POINTER(i64), ctypes.POINTER(i64),
@@ -225,6 +226,33 @@ def block_fwd(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=None, s
                                  _ptr(y), _ptr(rstd), ws.ptr, ws.nbytes, _stream(stream)),
            "boost_block_fwd")
     return y
+
+
+def block_fwd_swiglu(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, h=None, rstd=None,
+                     stream=None):
+    """Gate/up block (k == 2) forward with the SwiGLU forward fused in: returns
+    (y [2,T,n] = gate, up; h [T,n] = silu(gate) * up)."""
+    bf = torch.bfloat16
+    if desc.k != 2:
+        raise ValueError("block_fwd_swiglu needs k == 2 (gate and up groups)")
+    _need(x, "x", bf, (desc.T, desc.d))
+    _need(A, "A", bf, (desc.d, desc.k * desc.r))
+    _need(B, "B", bf, (desc.k, desc.r, desc.n))
+    if desc.has_norm:
+        _need(gamma, "gamma", bf, (desc.d,))
+    if y is None:
+        y = torch.empty(desc.k, desc.T, desc.n, dtype=bf, device=x.device)
+    if h is None:
+        h = torch.empty(desc.T, desc.n, dtype=bf, device=x.device)
+    _need(y, "y", bf, (desc.k, desc.T, desc.n))
+    _need(h, "h", bf, (desc.T, desc.n))
+    if rstd is not None:
+        _need(rstd, "rstd", torch.float32, (desc.T,))
+    _check(lib().boost_block_fwd_swiglu(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(A),
+                                        _ptr(B), _ptr(y), _ptr(h), _ptr(rstd), ws.ptr, ws.nbytes,
+                                        _stream(stream)),
+           "boost_block_fwd_swiglu")
+    return y, h
 
 
 def block_bwd(desc: Desc, x, gamma, A, B, dy, ws: Workspace, *, rstd=None, dx=None,

@@ -57,7 +57,8 @@ class MLP:
                  device="cuda", ws=None, fused_glu=True):
         w = weights or {}
         self.T, self.d, self.ffn = T, d, ffn
-        # backward of the down block with the SwiGLU backward in its dgrad epilogue
+        # SwiGLU forward in the gate/up up-projection's epilogue, and its backward in the
+        # down block's dgrad epilogue (False: separate SwiGLU passes)
         self.fused_glu = fused_glu
         self.gu = Block(T, d, r, 2, ffn, S=S, eps=eps, act=act, has_norm=True,
                         weights={"gamma": w.get("gamma"), "A": w.get("A1"), "B": w.get("B1")},
@@ -75,8 +76,13 @@ class MLP:
         return self.dn.y[0]
 
     def forward(self, x, stream=None):
-        y1 = self.gu.forward(x, stream)
-        B.swiglu_fwd(y1[0], y1[1], self.h, stream=stream)
+        if self.fused_glu:
+            gu = self.gu
+            B.block_fwd_swiglu(gu.desc, x, gu.gamma, gu.A, gu.B, gu.ws, y=gu.y, h=self.h,
+                               rstd=gu.rstd, stream=stream)
+        else:
+            y1 = self.gu.forward(x, stream)
+            B.swiglu_fwd(y1[0], y1[1], self.h, stream=stream)
         return self.dn.forward(self.h, stream)[0]
 
     def backward(self, x, dout, stream=None):

@@ -30,13 +30,13 @@ int gemm_resident_bwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms);
 
 cudaError_t launch_gemm(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
-  if (mode == EPI_ACT || mode == EPI_BF16)
+  if (mode == EPI_ACT || mode == EPI_BF16 || mode == EPI_UPGLU)
     return launch_gemm_fwd_modes(bn, mode, cg, mcm, mcn, p, num_sms, stream);
   return launch_gemm_bwd_modes(bn, mode, cg, mcm, mcn, p, num_sms, stream);
 }
 
 int gemm_resident(int bn, int mode, int cg, int mcm, int mcn, int num_sms) {
-  if (mode == EPI_ACT || mode == EPI_BF16)
+  if (mode == EPI_ACT || mode == EPI_BF16 || mode == EPI_UPGLU)
     return gemm_resident_fwd(bn, mode, cg, mcm, mcn, num_sms);
   return gemm_resident_bwd(bn, mode, cg, mcm, mcn, num_sms);
 }
@@ -106,9 +106,11 @@ EncodeFn get_encode() {
 }
 
 // 3-D bf16 view: dims (d0 contiguous, d1, d2), byte strides of d1 and d2, box b0 x b1 x b2,
-// 128-byte swizzle, zero fill out of bounds.
+// 128-byte swizzle (operand loads) or 64-byte swizzle (32-wide epilogue store boxes),
+// zero fill out of bounds.
 bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+              bool sw64 = false) {
   EncodeFn enc = get_encode();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {d0, d1, d2};
@@ -116,9 +118,27 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Maps for the epilogue's TMA stores (the SwiGLU epilogue modes store through TMA; the
+// others use plain stores and need none): out (`batches` matrices of rows x cols,
+// out_bstride apart) and out2 (`batches2` of them), leading dimension ldo, 32 x 32
+// boxes. An output whose map cannot be made is written with plain stores.
+void set_out_maps(GemmParams& g, int64_t rows, int64_t cols, int64_t batches,
+                  int64_t batches2 = 1) {
+  const uint64_t ld = static_cast<uint64_t>(g.ldo) * 2;
+  if (g.out != nullptr &&
+      make_map(&g.tmO[0], g.out, cols, rows, batches, ld,
+               (batches > 1 ? static_cast<uint64_t>(g.out_bstride) : rows * g.ldo) * 2, 32, 32, 1,
+               true))
+    g.tma_out |= 1;
+  if (g.out2 != nullptr &&
+      make_map(&g.tmO[1], g.out2, cols, rows, batches2, ld, rows * g.ldo * 2, 32, 32, 1, true))
+    g.tma_out |= 2;
 }
 
 // A row-major [rows, cols] bf16 matrix (rows < 2^31), viewed 3-D as (cols, rows, 1).
@@ -458,16 +478,26 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x, fl
   return cuda_status(launch_rmsnorm_stats(x, desc->T, desc->d, desc->S, desc->eps, ssq, rstd, s));
 }
 
-boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const void* gamma,
-                             const void* A, const void* B, void* y, float* rstd, void* ws,
-                             size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward of one block. With `h` non-NULL (k == 2: gate and up groups) the up-projection
+// computes both groups of a tile in one kernel and its epilogue also writes
+// h = silu(gate) * up.
+boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const void* gamma,
+                            const void* A, const void* B, void* y, void* h, bool glu,
+                            float* rstd, void* ws, size_t ws_bytes, void* stream) {
   boost_status st = validate_desc(desc);
   if (st != BOOST_OK) return st;
   const boost_block_desc& D = *desc;
   if (!D.has_norm && (gamma != nullptr || rstd != nullptr)) return BOOST_ERR_INVALID_ARG;
+  if (glu && D.k != 2) return BOOST_ERR_INVALID_ARG;
   // With no tokens the [T, ...] tensors are empty and may be NULL.
-  st = D.T == 0 ? check_ptrs({A, B}, {gamma, rstd, x, y}) : check_ptrs({x, A, B, y}, {gamma, rstd});
+  st = D.T == 0 ? check_ptrs({A, B}, {gamma, rstd, x, y, h})
+                : check_ptrs({x, A, B, y}, {gamma, rstd, h});
   if (st != BOOST_OK) return st;
+  if (glu && D.T > 0 && h == nullptr) return BOOST_ERR_INVALID_ARG;
   if (D.has_norm && gamma == nullptr) return BOOST_ERR_INVALID_ARG;
   const int sms = current_num_sms();
   const Plan P = make_plan(D, sms);
@@ -528,12 +558,43 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
   u.out = y;
   u.ldo = P.n;
   u.out_bstride = P.T * P.n;
-  {
+  if (glu) {
+    // one tile list; segment 0 = the gate group into accumulator 0, segment 1 = the up
+    // group (same maps, batch index + 1) into accumulator 1
+    u.batch = 1;
+    u.num_seg = 2;
+    u.seg[1] = u.seg[0];
+    u.seg[1].batch_add = 1;
+    u.tmA[1] = u.tmA[0];
+    u.tmB[1] = u.tmB[0];
+    u.out2 = h;
+    set_out_maps(u, P.T, P.n, 2, 1);
+    ProfScope ps(s, K_UP_GLU, 2.0 * P.T * P.kr * P.n,
+                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n + P.T * P.n));
+    e = launch_gemm_rows(P.up, EPI_UPGLU, u, sms, s);
+  } else {
     ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
     e = launch_gemm_rows(P.up, EPI_BF16, u, sms, s);
   }
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const void* gamma,
+                             const void* A, const void* B, void* y, float* rstd, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return block_fwd_impl(desc, x, gamma, A, B, y, nullptr, false, rstd, ws, ws_bytes, stream);
+}
+
+boost_status boost_block_fwd_swiglu(const boost_block_desc* desc, const void* x,
+                                    const void* gamma, const void* A, const void* B, void* y,
+                                    void* h, float* rstd, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  return block_fwd_impl(desc, x, gamma, A, B, y, h, true, rstd, ws, ws_bytes, stream);
 }
 
 }  // extern "C"
@@ -736,6 +797,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.gate = static_cast<const __nv_bfloat16*>(gate);
       w.up = static_cast<const __nv_bfloat16*>(up);
     }
+    if (glu) set_out_maps(w, P.T, P.d, 1, 1);
     if (D.has_norm) {
       w.rstd = rs;
       w.qpart = qpart;

@@ -53,6 +53,8 @@ enum EpiMode : int {
   EPI_DX = 4,      // out_bf16 = acc - (s^2 q / d) x            (dgrad x + RMSNorm bwd)
   EPI_DA = 5,      // out_bf16 = gamma_row * acc, dgamma partials (wgrad of A)
   EPI_GLU = 6,     // dh = bf16(acc); out = dh*up*silu'(gate), out2 = dh*silu(gate) (SwiGLU bwd)
+  EPI_UPGLU = 7,   // two accumulators: gate, up = bf16(acc0), bf16(acc1) to out[0], out[1];
+                   // out2 = h = bf16(silu(gate) * up)     (up-projection + SwiGLU fwd)
 };
 
 struct OperandView {
@@ -67,12 +69,14 @@ struct Segment {
   int32_t num_kb;        // k-blocks of 64 over the whole K of this segment
   int32_t batch_from_n;  // batch index = the tile's group instead of the tile's batch
   int32_t b_n_local;     // B operand's MN coordinate is the column within the group
-  int32_t pad;
+  int32_t batch_add;     // added to the batch index of both operands of this segment
 };
 
 struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
+  CUtensorMap tmO[2];         // bf16 outputs out / out2 as (cols, rows, batch), 32 x 32 boxes
+  int32_t tma_out;            // bit i: tmO[i] is valid (else plain stores)
   Segment seg[2];
   int32_t num_seg;
   int32_t M, N;               // output extent (per batch)
@@ -89,7 +93,7 @@ struct GemmParams {
   int32_t nq;                 // EPI_DX: number of q partial rows to sum
   // epilogue tensors (elements, not bytes, for strides)
   void* out;                  // bf16 or fp32 output
-  void* out2;                 // EPI_DUAL: dzs
+  void* out2;                 // EPI_DUAL: dzs; EPI_GLU: dup; EPI_UPGLU: h
   int64_t ldo;                // leading dimension of out/out2
   int64_t out_bstride;        // batch stride of out
   int64_t out_sstride;        // split stride of out (EPI_F32)
@@ -107,21 +111,41 @@ struct GemmParams {
 
 template <int BN, int MODE, int CG, int MCM = 1, int MCN = 1>
 struct GemmCfg {
-  static constexpr bool kDual = (MODE == EPI_DUAL);
+  // two accumulators per tile, one per segment
+  static constexpr bool kDual = (MODE == EPI_DUAL || MODE == EPI_UPGLU);
   static constexpr int kBRows = BN / CG;                          // B rows staged per CTA
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  // Epilogue output path. TMA stores (a ring of 2 KB slots per warp, one bulk store per
+  // 32 x 32 bf16 chunk) take the global write latency off the epilogue warps, which
+  // pays where the epilogue is the bottleneck (the SwiGLU epilogues); elsewhere they
+  // compete with the operand loads for the SM's TMA unit, and plain coalesced stores
+  // through the warp's staging block measured faster.
+  static constexpr bool kTmaStore = (MODE == EPI_GLU || MODE == EPI_UPGLU);
+  // Staging per warp: a load slot (2 KB, modes that read a bf16 operand) and the store
+  // slots; plain-store modes share one 4 KB block (fp32 partials use all of it).
+  static constexpr bool kLoads = (MODE == EPI_DX || MODE == EPI_DA || MODE == EPI_GLU);
+  static constexpr int kStoreSlots = (MODE == EPI_F32) ? 0 : (kTmaStore ? 2 : 1);
+  static constexpr int kLoadBytes = kTmaStore ? (kLoads ? 2048 : 0) : 0;
+  static constexpr int kWarpStg = kTmaStore ? kLoadBytes + 2048 * kStoreSlots : 4096;
+  static constexpr int kStgBytes = kEpiWarps * kWarpStg;
+  static constexpr int kStagesRaw = (232448 - 2048 - kStgBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kAccCols = kDual ? 2 * BN : BN;            // columns per accumulator set
   static constexpr int kAccStages = (2 * kAccCols <= 512) ? 2 : 1;
+  // EPI_UPGLU with one accumulator set: the epilogue frees the first accumulator (gate)
+  // before it reads the second, so the next tile's first segment overlaps the rest of
+  // the epilogue. One "empty" barrier per accumulator then.
+  static constexpr bool kSplitRelease = (MODE == EPI_UPGLU && kAccStages == 1);
+  static constexpr int kTemptyBars = kSplitRelease ? 2 : kAccStages;
   static constexpr int kTmemColsRaw = kAccStages * kAccCols;
   static constexpr int kTmemCols = kTmemColsRaw <= 32 ? 32 : kTmemColsRaw <= 64 ? 64
                                    : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kAccStages + 1) + 16;
-  static constexpr int kStgBytes = kEpiWarps * 4096;              // epilogue staging, 4 KB per warp
-  static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 127) / 128 * 128;
+  static constexpr int kBarBytes = 8 * (2 * kStages + kAccStages + kTemptyBars + 1) + 16;
+  // staging slots 1024-byte aligned (the 64-byte swizzle pattern of a TMA box repeats
+  // every 512 bytes)
+  static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStgOffset + kStgBytes;
   static constexpr int kMmaM = kBM * CG;                    // M of one tcgen05.mma
   static constexpr int kPairs = MCM * MCN;                  // pairs per cluster
@@ -351,16 +375,68 @@ __device__ __forceinline__ void stage_load_bf16(uint8_t* stg, int lane, const __
   __syncwarp();
 }
 
+// A warp's ring of 2 KB shared-memory slots for TMA stores of bf16 32 x 32 chunks. Only
+// lane 0 issues and tracks the stores (bulk groups are per thread).
+template <int kSlots, bool kTma>
+struct StoreRing {
+  uint8_t* base;
+  int next;
+};
+
+// Store this warp's 32 x 32 bf16 chunk (lane = row; pk = the row's 32 values, packed) at
+// column col0, row row0, batch `batch` of output map `tm`. The chunk goes through the
+// next slot of the ring (64-byte swizzled rows, the map's layout) and one TMA store,
+// which clips rows and columns outside the map; the warp does not wait for the global
+// write. With `tma` false (no map, or the chunk is cut by a group boundary inside the
+// tensor, which the map cannot clip) it is written with coalesced plain stores instead.
+template <int kSlots, bool kTma>
+__device__ __forceinline__ void store_chunk_bf16(StoreRing<kSlots, kTma>& ring, int lane,
+                                                 const uint32_t (&pk)[16], const CUtensorMap* tm,
+                                                 bool tma, int32_t col0, int32_t row0,
+                                                 int32_t batch, __nv_bfloat16* g, int64_t ld,
+                                                 int rows_valid, int cols_valid) {
+  if constexpr (!kTma) {
+    (void)tm; (void)tma; (void)col0; (void)row0; (void)batch;
+    stage_store_bf16(ring.base, lane, pk, g, ld, rows_valid, cols_valid);
+    return;
+  }
+  uint8_t* slot = ring.base + ring.next * 2048;
+  ring.next = ring.next + 1 == kSlots ? 0 : ring.next + 1;
+  if (tma) {
+    // the store that last used this slot was committed kSlots - 1 groups ago (or an
+    // intervening plain store already drained every group)
+    if (lane == 0) bulk_wait_group_read<kSlots - 1>();
+    __syncwarp();
+    uint4* mine = reinterpret_cast<uint4*>(slot + lane * 64);
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      mine[c ^ sw] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tm, slot, col0, row0, batch);
+      bulk_commit_group();
+    }
+  } else {
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    stage_store_bf16(slot, lane, pk, g, ld, rows_valid, cols_valid);
+  }
+}
+
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
 // `col_tile` indexes the per-row partial sums (q, dgamma) of this BN-wide column tile.
 // `half` selects the 32-column chunks of this warp (half, half + kEpiHalves, ...); the
 // per-row partial sums are written per half, at row col_tile * kEpiHalves + half.
-template <int BN, int MODE>
+// `stg` is the warp's load slot (fp32 staging for EPI_F32), `ring` its store slots.
+template <int BN, int MODE, int kSlots, bool kTma>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
                                               int32_t row0, int32_t n0, int32_t n_end,
-                                              uint32_t t_row, uint8_t* stg, int lane,
+                                              uint32_t t_row, uint8_t* stg,
+                                              StoreRing<kSlots, kTma>& ring, int lane,
                                               int32_t col_tile, int half) {
   const int32_t row = row0 + lane;
   const bool row_ok = row < p.M;
@@ -395,6 +471,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     const int32_t col0 = n0 + c * 32;
     const int cols_valid = n_end - col0;
     if (cols_valid <= 0) break;            // warp-uniform: the rest of the tile is outside N
+    const bool whole = cols_valid >= 32 || n_end == p.N;   // the maps clip at N only
     float v[32];
     tmem_ld_32x32b_x32(t_row + c * 32, v);
     float w[32];
@@ -440,7 +517,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         }
         __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
                             static_cast<int64_t>(row0) * p.ldo + col0;
-        stage_store_bf16(stg, lane, pk2, o2, p.ldo, rows_valid, cols_valid);
+        store_chunk_bf16(ring, lane, pk2, &p.tmO[1], whole && (p.tma_out & 2), col0, row0, 0, o2,
+                         p.ldo, rows_valid, cols_valid);
       } else if constexpr (MODE == EPI_GLU) {
         // SwiGLU backward on the down-projection's input gradient dh (rounded to bf16,
         // the value a separate pass would have stored): dgate and dup of h = silu(g)*u.
@@ -471,7 +549,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         }
         __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
                             static_cast<int64_t>(row0) * p.ldo + col0;
-        stage_store_bf16(stg, lane, pk2, o2, p.ldo, rows_valid, cols_valid);
+        store_chunk_bf16(ring, lane, pk2, &p.tmO[1], whole && (p.tma_out & 2), col0, row0, 0, o2,
+                         p.ldo, rows_valid, cols_valid);
       } else if constexpr (MODE == EPI_DX) {
         float xv[32];
         if (__any_sync(0xffffffffu, coef != 0.0f)) {   // warp-uniform: the load is cooperative
@@ -498,7 +577,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       }
       __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
                          static_cast<int64_t>(row0) * p.ldo + col0;
-      stage_store_bf16(stg, lane, pk, o, p.ldo, rows_valid, cols_valid);
+      store_chunk_bf16(ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
+                       o, p.ldo, rows_valid, cols_valid);
     }
   }
   if constexpr (MODE == EPI_DUAL) {
@@ -508,6 +588,71 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   if constexpr (MODE == EPI_DA) {
     if (row_ok && p.dgpart != nullptr)
       p.dgpart[static_cast<int64_t>(col_tile * kEpiHalves + half) * p.M + row] = rowsum;
+  }
+}
+
+// silu(g) * u on bf16 gate and up values, the same expression (and the same sigmoid) as
+// the stand-alone SwiGLU forward kernel, so that the fused and the separate paths give
+// identical h.
+__device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoid_f(g) * u; }
+
+// Epilogue of the fused up-projection + SwiGLU forward for the calling warp (rows
+// [row0, row0 + 32), columns [n0, n_end), the 32-column chunks half, half + kEpiHalves,
+// ...). Accumulator 0 (gate, TMEM columns [0, BN)) is read first, rounded to bf16, kept
+// in registers and stored; then, if `release0` is set, this warp's arrival on it lets
+// the MMA warp start the next tile's gate segment while accumulator 1 (up, columns
+// [BN, 2 BN)) is read and up and h = silu(gate) * up are stored.
+template <int BN, int CG, int kSlots, bool kTma>
+__device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0, int32_t n0,
+                                               int32_t n_end, uint32_t t_row,
+                                               StoreRing<kSlots, kTma>& ring, int lane, int half,
+                                               uint64_t* release0, uint32_t leader_rank) {
+  constexpr int kChunks = BN / 32 / kEpiHalves;
+  const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
+  __nv_bfloat16* y0 = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row0) * p.ldo;
+  __nv_bfloat16* y1 = y0 + p.out_bstride;
+  __nv_bfloat16* hh = static_cast<__nv_bfloat16*>(p.out2) + static_cast<int64_t>(row0) * p.ldo;
+  uint32_t gk[kChunks][16];
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
+    if (col0 < n_end) {                     // warp-uniform
+      float v[32];
+      tmem_ld_32x32b_x32(t_row + (half + j * kEpiHalves) * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) gk[j][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 0,
+                       y0 + col0, p.ldo, rows_valid, n_end - col0);
+    }
+  }
+  if (release0 != nullptr) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(release0), leader_rank));
+      else mbar_arrive(release0);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
+    if (col0 < n_end) {                     // warp-uniform
+      float w[32];
+      tmem_ld_32x32b_x32(t_row + BN + (half + j * kEpiHalves) * 32, w);
+      tmem_ld_wait();
+      uint32_t uk[16], hk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uk[i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
+        hk[i] = pack_bf16x2(swiglu_h(bf16_lo(gk[j][i]), bf16_lo(uk[i])),
+                            swiglu_h(bf16_hi(gk[j][i]), bf16_hi(uk[i])));
+      }
+      store_chunk_bf16(ring, lane, uk, &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 1,
+                       y1 + col0, p.ldo, rows_valid, n_end - col0);
+      store_chunk_bf16(ring, lane, hk, &p.tmO[1], (p.tma_out & 2) != 0, col0, row0, 0,
+                       hh + col0, p.ldo, rows_valid, n_end - col0);
+    }
   }
 }
 
@@ -525,7 +670,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint64_t* empty_bar = full_bar + Cfg::kStages;
   uint64_t* tfull_bar = empty_bar + Cfg::kStages;
   uint64_t* tempty_bar = tfull_bar + Cfg::kAccStages;
-  uint64_t* done_bar = tempty_bar + Cfg::kAccStages;
+  uint64_t* done_bar = tempty_bar + Cfg::kTemptyBars;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -546,10 +691,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(&full_bar[s], 1);           // the even CTA's expect_tx covers both CTAs
       mbar_init(&empty_bar[s], Cfg::kPairs);  // freed once every pair of the cluster is done
     }
-    for (int s = 0; s < Cfg::kAccStages; ++s) {
-      mbar_init(&tfull_bar[s], 1);
+    for (int s = 0; s < Cfg::kAccStages; ++s) mbar_init(&tfull_bar[s], 1);
+    for (int s = 0; s < Cfg::kTemptyBars; ++s)
       mbar_init(&tempty_bar[s], kEpiWarps * CG);   // one arrival per epilogue warp of the pair
-    }
     mbar_init(done_bar, 1);
     fence_barrier_init();
   }
@@ -592,6 +736,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           int32_t b = tc.batch;
           int32_t nb = tc.n0;
           if (S.batch_from_n) b = tc.group;
+          b += S.batch_add;
           if (S.b_n_local) nb = tc.n_local;
           int32_t kb0, kb1;
           kb_range(p, sg, tc.split, kb0, kb1);
@@ -671,12 +816,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const uint32_t sB_u32 = smem_u32(sB);
       for (int32_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
         const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
-        if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
-          ok = false;
-          break;
+        if constexpr (!Cfg::kSplitRelease) {
+          if (!bounded_wait(&tempty_bar[acc], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
         for (int sg = 0; sg < p.num_seg && ok; ++sg) {
+          if constexpr (Cfg::kSplitRelease) {
+            // segment sg accumulates into accumulator sg: wait until it has been read
+            if (!bounded_wait(&tempty_bar[sg], acc_phase ^ 1u, p.err, 2, p.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols + sg * BN;
           const int a_mn = p.seg[sg].a.mn_major, b_mn = p.seg[sg].b.mn_major;
           const uint32_t idesc = sg == 0 ? idesc0 : idesc1;
@@ -737,7 +892,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                    // TMEM lane quarter of this warp
     const int half = (warp - 2) / 4;           // which alternate column chunks it takes
-    uint8_t* stg = smem + Cfg::kStgOffset + (warp - 2) * 4096;
+    uint8_t* stg = smem + Cfg::kStgOffset + (warp - 2) * Cfg::kWarpStg;
+    StoreRing<Cfg::kStoreSlots, Cfg::kTmaStore> ring{stg + Cfg::kLoadBytes, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
@@ -751,19 +907,31 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // this pair's columns of the super-tile (may be empty past the group or N end)
       const int32_t pn0 = tc.n0 + static_cast<int32_t>(pn) * BN;
       const int32_t pend = min(pn0 + BN, tc.n_end);
-      epilogue_tile<BN, MODE>(p, tc, row0, pn0, pend, t_row, stg, lane,
-                              tc.n_blk * MCN + static_cast<int32_t>(pn), half);
+      if constexpr (MODE == EPI_UPGLU) {
+        epilogue_upglu<BN, CG, Cfg::kStoreSlots, Cfg::kTmaStore>(
+            p, row0, pn0, pend, t_row, ring, lane, half,
+            Cfg::kSplitRelease ? &tempty_bar[0] : nullptr, leader_rank);
+      } else {
+        epilogue_tile<BN, MODE, Cfg::kStoreSlots, Cfg::kTmaStore>(
+            p, tc, row0, pn0, pend, t_row, stg, ring, lane,
+            tc.n_blk * MCN + static_cast<int32_t>(pn), half);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (CG == 2)
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), leader_rank));
-        else mbar_arrive(&tempty_bar[acc]);
+        uint64_t* bar = &tempty_bar[Cfg::kSplitRelease ? 1 : acc];
+        if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(bar), leader_rank));
+        else mbar_arrive(bar);
       }
       if (++acc == Cfg::kAccStages) {
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    // this warp's TMA stores have read their slots and written global memory
+    if constexpr (Cfg::kTmaStore) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
     }
   }
 

@@ -1,6 +1,7 @@
 // gemm_fwd.cu -- instantiations of the tensor-core GEMM for the forward path:
 // the grouped down-projection with deferred 1/rms + activation (EPI_ACT) and plain
-// bf16 stores (EPI_BF16: batched up-projection, unsplit dB).
+// bf16 stores (EPI_BF16: batched up-projection, unsplit dB), and the gate/up
+// up-projection with the SwiGLU forward in its epilogue (EPI_UPGLU).
 #include "gemm_launch.inc"
 
 namespace boost_gb300 {
@@ -9,12 +10,14 @@ cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mcm, int mcn, co
                                   cudaStream_t stream) {
   if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, mcm, mcn, p, num_sms, stream);
   if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, mcm, mcn, p, num_sms, stream);
+  if (mode == EPI_UPGLU) return launch_mode<EPI_UPGLU>(bn, cg, mcm, mcn, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 
 int gemm_resident_fwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms) {
   if (mode == EPI_ACT) return resident_mode<EPI_ACT>(bn, cg, mcm, mcn, num_sms);
   if (mode == EPI_BF16) return resident_mode<EPI_BF16>(bn, cg, mcm, mcn, num_sms);
+  if (mode == EPI_UPGLU) return resident_mode<EPI_UPGLU>(bn, cg, mcm, mcn, num_sms);
   return num_sms / cg;
 }
 

@@ -31,10 +31,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// logistic(z) with the hardware exp2 and a fast reciprocal divide, the same expression
+// as the GEMM epilogues', so that the fused and the stand-alone SwiGLU passes agree bit
+// for bit.
+__device__ __forceinline__ float sigmoid_fast(float z) {
+  return __fdividef(1.0f, 1.0f + __expf(-z));
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z * sigmoid_fast(z); }
 
 __device__ __forceinline__ float silu_grad_f(float z) {
-  const float g = 1.0f / (1.0f + __expf(-z));
+  const float g = sigmoid_fast(z);
   return g * (1.0f + z * (1.0f - g));
 }
 

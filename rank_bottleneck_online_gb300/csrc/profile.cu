@@ -18,7 +18,8 @@ const char* const kNames[K_COUNT] = {
     "rmsnorm_stats", "fold_gamma",     "gemm_down_act",  "gemm_up",
     "gemm_dual",     "gemm_wgrad_B",   "gemm_wgrad_A",   "gemm_dx",
     "splitk_sum",    "splitk_finalize_dA", "dgamma_reduce", "swiglu_fwd",
-    "swiglu_bwd",    "add",            "wait_probe",    "gemm_dx_swiglu"};
+    "swiglu_bwd",    "add",            "wait_probe",    "gemm_dx_swiglu",
+    "gemm_up_swiglu"};
 
 struct Pending {
   int id;

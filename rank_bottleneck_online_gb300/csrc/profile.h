@@ -24,6 +24,7 @@ enum KernelId : int {
   K_ADD,
   K_PROBE,
   K_DX_GLU,
+  K_UP_GLU,
   K_COUNT
 };
 

@@ -129,6 +129,19 @@ def test_bwd_argument_checks(L):
     assert st == 3                                             # misaligned dy
 
 
+def test_fused_swiglu_forward_argument_checks(L):
+    f = _fake
+
+    def fwd_glu(desc, h):
+        return L.boost_block_fwd_swiglu(ctypes.byref(desc), f(0x1000), f(0x2000), f(0x3000),
+                                        f(0x4000), f(0x5000), h, None, f(0x100000), 1 << 30,
+                                        None)
+
+    assert fwd_glu(B.make_desc(128, 256, 64, 3, 256, S=4), f(0x6000)) == 1   # k must be 2
+    assert fwd_glu(B.make_desc(128, 256, 64, 2, 256, S=4), None) == 1        # h missing
+    assert fwd_glu(B.make_desc(128, 256, 64, 2, 256, S=4), f(0x6008)) == 3   # h misaligned
+
+
 def test_elementwise_argument_checks(L):
     assert L.boost_swiglu_fwd(4, 12, _fake(0x1000), _fake(0x2000), _fake(0x3000), None) == 2
     assert L.boost_swiglu_fwd(-1, 8, _fake(0x1000), _fake(0x2000), _fake(0x3000), None) == 1

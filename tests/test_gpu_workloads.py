@@ -65,6 +65,30 @@ def test_fused_swiglu_backward_matches_separate_passes(T, d, r, ffn):
         assert_close(k, g_f[k], g_s[k].double().cpu().numpy(), 1e-2, 1e-3)
 
 
+@pytest.mark.parametrize("T,d,r,n", [(512, 256, 128, 512), (600, 128, 64, 520), (300, 128, 64, 200),
+                                     (4352, 256, 128, 1024)])
+def test_fused_swiglu_forward_matches_separate_passes(T, d, r, n):
+    # the gate/up up-projection with two accumulators and SwiGLU in its epilogue gives
+    # the batched up-projection's gate and up bit for bit, and the stand-alone SwiGLU
+    # pass's h bit for bit (same MMAs, same K order, same expression). Shapes: 2 x 2
+    # clusters with one accumulator set (early release of the gate accumulator), a
+    # ragged last column tile, 128-wide double-buffered tiles, co-scheduled rows.
+    w = inputs.make_block(T, d, r, 2, n, seed=7)
+    blk = Block(T, d, r, 2, n, S=4, weights=w)
+    x = w["x"].cuda()
+    y_sep = blk.forward(x).clone()
+    h_sep = torch.empty(T, n, dtype=torch.bfloat16, device="cuda")
+    B.swiglu_fwd(y_sep[0], y_sep[1], h_sep)
+    y = torch.full_like(y_sep, float("nan"))
+    y_f, h_f = B.block_fwd_swiglu(blk.desc, x, blk.gamma, blk.A, blk.B, blk.ws, y=y)
+    B.check(blk.ws)
+    assert torch.equal(y_f, y_sep)
+    assert torch.equal(h_f, h_sep)
+    # and against the oracle: h from the bf16 gate and up
+    o = oracle.swiglu_fwd(inputs.as_f64(y_sep[0].cpu()), inputs.as_f64(y_sep[1].cpu()))
+    assert_close("h", h_f, o)
+
+
 def test_layer_parity():
     T, d, r, ffn, S = 256, 256, 64, 384, 4
     w = inputs.make_layer(T, d, r, ffn, seed=2)
