@@ -33,6 +33,7 @@
 
 #include <cuda.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -76,7 +77,9 @@ struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
   CUtensorMap tmO[2];         // bf16 outputs out / out2 as (cols, rows, batch), 32 x 32 boxes
+  CUtensorMap tmE[2];         // bf16 epilogue inputs (EPI_GLU: gate, up; EPI_DX: x), 32 x 32
   int32_t tma_out;            // bit i: tmO[i] is valid (else plain stores)
+  int32_t tma_in;             // 1: the epilogue inputs stream through tmE (EPI_GLU: required)
   Segment seg[2];
   int32_t num_seg;
   int32_t M, N;               // output extent (per batch)
@@ -123,12 +126,20 @@ struct GemmCfg {
   // compete with the operand loads for the SM's TMA unit, and plain coalesced stores
   // through the warp's staging block measured faster.
   static constexpr bool kTmaStore = (MODE == EPI_GLU || MODE == EPI_UPGLU);
-  // Staging per warp: a load slot (2 KB, modes that read a bf16 operand) and the store
-  // slots; plain-store modes share one 4 KB block (fp32 partials use all of it).
-  static constexpr bool kLoads = (MODE == EPI_DX || MODE == EPI_DA || MODE == EPI_GLU);
+  // Epilogue inputs streamed by TMA (EpiLoader): gate and up for EPI_GLU, x for EPI_DX,
+  // kEpiDepth chunks ahead of the consumer.
+  static constexpr int kEpiStreams = (MODE == EPI_GLU) ? 2 : (MODE == EPI_DX ? 1 : 0);
+  // (one chunk ahead where two would leave the mainloop fewer than three stages: the
+  // single-CTA 256-wide tile with two streams)
+  static constexpr int kEpiDepth = (kEpiStreams == 2 && kStageBytes >= 48 * 1024) ? 1 : 2;
+  // Staging per warp: load slots (the loader's kEpiDepth x kEpiStreams 2 KB slots, or one
+  // 2 KB slot for EPI_DA's synchronous loads), then the store slots (2 KB each); fp32
+  // partials use one 4 KB block.
   static constexpr int kStoreSlots = (MODE == EPI_F32) ? 0 : (kTmaStore ? 2 : 1);
-  static constexpr int kLoadBytes = kTmaStore ? (kLoads ? 2048 : 0) : 0;
-  static constexpr int kWarpStg = kTmaStore ? kLoadBytes + 2048 * kStoreSlots : 4096;
+  static constexpr int kLoadBytes =
+      kEpiStreams > 0 ? kEpiDepth * kEpiStreams * 2048 : (MODE == EPI_DA ? 2048 : 0);
+  static constexpr int kWarpStg = (MODE == EPI_F32) ? 4096 : kLoadBytes + 2048 * kStoreSlots;
+  static constexpr int kLdBars = kEpiStreams > 0 ? kEpiWarps * kEpiDepth : 0;
   static constexpr int kStgBytes = kEpiWarps * kWarpStg;
   static constexpr int kStagesRaw = (232448 - 2048 - kStgBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
@@ -142,7 +153,8 @@ struct GemmCfg {
   static constexpr int kTmemColsRaw = kAccStages * kAccCols;
   static constexpr int kTmemCols = kTmemColsRaw <= 32 ? 32 : kTmemColsRaw <= 64 ? 64
                                    : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
-  static constexpr int kBarBytes = 8 * (2 * kStages + kAccStages + kTemptyBars + 1) + 16;
+  static constexpr int kBarBytes =
+      8 * (2 * kStages + kAccStages + kTemptyBars + 1 + kLdBars) + 16;
   // staging slots 1024-byte aligned (the 64-byte swizzle pattern of a TMA box repeats
   // every 512 bytes)
   static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 1023) / 1024 * 1024;
@@ -312,42 +324,6 @@ __device__ __forceinline__ void stage_store_f32(uint8_t* stg, int lane, const fl
   __syncwarp();
 }
 
-// Two halves of a coalesced 32 x 32 bf16 block read, so a caller can start the global
-// loads of the next block before finishing the current one: issue reads this lane's
-// four 16-byte pieces (rows 8j + lane/4, chunk lane%4) into registers; finish passes
-// them through the staging block and returns this lane's row in fp32.
-__device__ __forceinline__ void stage_issue_bf16(int lane, const __nv_bfloat16* g, int64_t ld,
-                                                 int rows_valid, int cols_valid, uint4 (&q)[4]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 8 * j + (lane >> 2), c = lane & 3;
-    q[j] = make_uint4(0, 0, 0, 0);
-    if (r < rows_valid && c * 8 < cols_valid)
-      q[j] = *reinterpret_cast<const uint4*>(g + static_cast<int64_t>(r) * ld + c * 8);
-  }
-}
-
-__device__ __forceinline__ void stage_finish_bf16(uint8_t* stg, int lane, const uint4 (&q)[4],
-                                                  float (&out)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 8 * j + (lane >> 2), c = lane & 3;
-    reinterpret_cast<uint4*>(stg + r * 64)[c ^ ((r >> 1) & 3)] = q[j];
-  }
-  __syncwarp();
-  const uint4* mine = reinterpret_cast<const uint4*>(stg + lane * 64);
-  const int sw = (lane >> 1) & 3;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 u = mine[c ^ sw];
-    out[8 * c + 0] = bf16_lo(u.x); out[8 * c + 1] = bf16_hi(u.x);
-    out[8 * c + 2] = bf16_lo(u.y); out[8 * c + 3] = bf16_hi(u.y);
-    out[8 * c + 4] = bf16_lo(u.z); out[8 * c + 5] = bf16_hi(u.z);
-    out[8 * c + 6] = bf16_lo(u.w); out[8 * c + 7] = bf16_hi(u.w);
-  }
-  __syncwarp();
-}
-
 // Coalesced read of a 32 x 32 bf16 block (row r at g + r*ld), delivered as this lane's
 // row in fp32; out-of-range rows or columns read as zero.
 __device__ __forceinline__ void stage_load_bf16(uint8_t* stg, int lane, const __nv_bfloat16* g,
@@ -425,19 +401,109 @@ __device__ __forceinline__ void store_chunk_bf16(StoreRing<kSlots, kTma>& ring, 
   }
 }
 
+// Read this lane's row (32 bf16 values, 64-byte swizzled 32 x 32 block) as fp32.
+__device__ __forceinline__ void slot_row_f32(const uint8_t* slot, int lane, float (&out)[32]) {
+  const uint4* mine = reinterpret_cast<const uint4*>(slot + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = mine[c ^ sw];
+    out[8 * c + 0] = bf16_lo(u.x); out[8 * c + 1] = bf16_hi(u.x);
+    out[8 * c + 2] = bf16_lo(u.y); out[8 * c + 3] = bf16_hi(u.y);
+    out[8 * c + 4] = bf16_lo(u.z); out[8 * c + 5] = bf16_hi(u.z);
+    out[8 * c + 6] = bf16_lo(u.w); out[8 * c + 7] = bf16_hi(u.w);
+  }
+}
+
+// Per-warp stream of the epilogue's bf16 inputs (kStreams tensors shaped like the
+// output, e.g. gate and up): for every 32 x 32 chunk the warp will write, in the order
+// it writes them and across tile boundaries, one TMA load per tensor into a ring of
+// kDepth slots, kDepth chunks ahead of the consumer. The loads do not depend on the
+// accumulator, so the next tile's first chunks are in flight before its MMAs finish.
+// Lane 0 issues; every lane waits on the slot's mbarrier (bounded) before reading.
+template <int BN, int TILE_N, int TILE_M, int kStreams, int kDepth>
+struct EpiLoader {
+  static constexpr int kChunks = BN / 32 / kEpiHalves;
+  static constexpr int kSlotBytes = kStreams * 2048;
+  const GemmParams* p;
+  uint8_t* slots;          // kDepth slots of kStreams 2 KB blocks
+  uint64_t* bars;          // kDepth mbarriers of this warp
+  int32_t tile, tile_stride, num_tiles;   // issue cursor: next tile ...
+  int j;                                  // ... and chunk index within it
+  int32_t row_off, col_off;               // this warp's rows / this pair's columns in a tile
+  int half;
+  uint32_t issued, consumed;
+
+  // Issue the loads of the next chunk this warp will write (if any) into the next slot.
+  __device__ __forceinline__ void issue_next(int lane) {
+    while (tile < num_tiles) {
+      const TileCoord tc = decode_tile<TILE_N, TILE_M>(*p, tile);
+      const int32_t pn0 = tc.n0 + col_off;
+      const int32_t col0 = pn0 + (half + j * kEpiHalves) * 32;
+      if (j < kChunks && col0 < min(pn0 + BN, tc.n_end)) {
+        const uint32_t slot = issued % kDepth;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[slot], kSlotBytes);
+#pragma unroll
+          for (int t = 0; t < kStreams; ++t)
+            tma_load_3d(slots + slot * kSlotBytes + t * 2048, &p->tmE[t], &bars[slot], col0,
+                        tc.m0 + row_off, 0);
+        }
+        ++issued;
+        ++j;
+        return;
+      }
+      tile += tile_stride;   // the rest of this tile's chunks lie past its columns
+      j = 0;
+    }
+  }
+
+  __device__ __forceinline__ void start(int lane) {
+    for (int d = 0; d < kDepth; ++d) issue_next(lane);
+  }
+
+  // The inputs of the warp's next chunk, one row per lane; then refill the slot.
+  __device__ __forceinline__ void consume(int lane, float (&out)[kStreams][32]) {
+    const uint32_t slot = consumed % kDepth;
+    bounded_wait(&bars[slot], (consumed / kDepth) & 1u, p->err, 9, p->wait_limit_ns);
+#pragma unroll
+    for (int t = 0; t < kStreams; ++t) slot_row_f32(slots + slot * kSlotBytes + t * 2048, lane, out[t]);
+    ++consumed;
+    fence_proxy_async_smem();   // these reads precede the next TMA write into the slot
+    __syncwarp();
+    issue_next(lane);
+  }
+
+  // Wait for loads still in flight (only after an early exit from the tile loop).
+  __device__ __forceinline__ void drain() {
+    while (consumed < issued) {
+      const uint32_t slot = consumed % kDepth;
+      bounded_wait(&bars[slot], (consumed / kDepth) & 1u, p->err, 10, p->wait_limit_ns);
+      ++consumed;
+    }
+  }
+};
+
+// Stand-in for modes without streamed inputs.
+struct NoLoader {
+  __device__ __forceinline__ void start(int) {}
+  __device__ __forceinline__ void drain() {}
+};
+
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
 // `col_tile` indexes the per-row partial sums (q, dgamma) of this BN-wide column tile.
 // `half` selects the 32-column chunks of this warp (half, half + kEpiHalves, ...); the
 // per-row partial sums are written per half, at row col_tile * kEpiHalves + half.
-// `stg` is the warp's load slot (fp32 staging for EPI_F32), `ring` its store slots.
-template <int BN, int MODE, int kSlots, bool kTma>
+// `stg` is the warp's load slot (fp32 staging for EPI_F32), `ring` its store slots, `ld`
+// its input stream (EPI_GLU, EPI_DX).
+template <int BN, int MODE, int kSlots, bool kTma, class Loader>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
                                               int32_t row0, int32_t n0, int32_t n_end,
                                               uint32_t t_row, uint8_t* stg,
-                                              StoreRing<kSlots, kTma>& ring, int lane,
-                                              int32_t col_tile, int half) {
+                                              StoreRing<kSlots, kTma>& ring, Loader& ld,
+                                              int lane, int32_t col_tile, int half) {
   const int32_t row = row0 + lane;
   const bool row_ok = row < p.M;
   const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
@@ -457,14 +523,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   float g_row = 1.0f;
   if constexpr (MODE == EPI_DA) {
     if (p.gamma != nullptr && row_ok) g_row = __bfloat162float(p.gamma[row]);
-  }
-  uint4 gq[4], uq[4];   // EPI_GLU: gate / up pieces of the next 32-column chunk, in flight
-  if constexpr (MODE == EPI_GLU) {
-    const int32_t c0 = n0 + half * 32;
-    stage_issue_bf16(lane, p.gate + static_cast<int64_t>(row0) * p.ldo + c0, p.ldo, rows_valid,
-                     n_end - c0, gq);
-    stage_issue_bf16(lane, p.up + static_cast<int64_t>(row0) * p.ldo + c0, p.ldo, rows_valid,
-                     n_end - c0, uq);
   }
 #pragma unroll 1
   for (int c = half; c < BN / 32; c += kEpiHalves) {
@@ -522,16 +580,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       } else if constexpr (MODE == EPI_GLU) {
         // SwiGLU backward on the down-projection's input gradient dh (rounded to bf16,
         // the value a separate pass would have stored): dgate and dup of h = silu(g)*u.
-        float gv[32], uv[32];
-        stage_finish_bf16(stg, lane, gq, gv);
-        stage_finish_bf16(stg, lane, uq, uv);
-        const int32_t nxt = col0 + 32 * kEpiHalves;   // this warp's next chunk
-        if (c + kEpiHalves < BN / 32 && nxt < n_end) {   // warp-uniform: prefetch it
-          stage_issue_bf16(lane, p.gate + static_cast<int64_t>(row0) * p.ldo + nxt, p.ldo,
-                           rows_valid, n_end - nxt, gq);
-          stage_issue_bf16(lane, p.up + static_cast<int64_t>(row0) * p.ldo + nxt, p.ldo,
-                           rows_valid, n_end - nxt, uq);
-        }
+        float gu[2][32];   // gate, up
+        ld.consume(lane, gu);
         uint32_t pk2[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -539,9 +589,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const float dh = __bfloat162float(__float2bfloat16_rn(v[i + h]));
-            const float z = gv[i + h];
+            const float z = gu[0][i + h];
             const float sg = sigmoid_f(z);
-            dgo[h] = dh * uv[i + h] * (sg * (1.0f + z * (1.0f - sg)));
+            dgo[h] = dh * gu[1][i + h] * (sg * (1.0f + z * (1.0f - sg)));
             duo[h] = dh * (z * sg);
           }
           pk[i / 2] = pack_bf16x2(dgo[0], dgo[1]);
@@ -552,17 +602,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         store_chunk_bf16(ring, lane, pk2, &p.tmO[1], whole && (p.tma_out & 2), col0, row0, 0, o2,
                          p.ldo, rows_valid, cols_valid);
       } else if constexpr (MODE == EPI_DX) {
-        float xv[32];
-        if (__any_sync(0xffffffffu, coef != 0.0f)) {   // warp-uniform: the load is cooperative
-          stage_load_bf16(stg, lane, p.xin + static_cast<int64_t>(row0) * p.ldo + col0, p.ldo,
-                          rows_valid, cols_valid, xv);
-        } else {
+        float xv[1][32];
+        if (p.tma_in) {                          // RMSNorm term: x streamed by the loader
+          ld.consume(lane, xv);
+        } else {                                 // no norm: coef == 0
 #pragma unroll
-          for (int i = 0; i < 32; ++i) xv[i] = 0.0f;
+          for (int i = 0; i < 32; ++i) xv[0][i] = 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(v[2 * i] - coef * xv[2 * i], v[2 * i + 1] - coef * xv[2 * i + 1]);
+          pk[i] = pack_bf16x2(v[2 * i] - coef * xv[0][2 * i],
+                              v[2 * i + 1] - coef * xv[0][2 * i + 1]);
       } else if constexpr (MODE == EPI_DA) {
         if (p.wA != nullptr) {
           float av[32];
@@ -598,10 +648,10 @@ __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoid
 
 // Epilogue of the fused up-projection + SwiGLU forward for the calling warp (rows
 // [row0, row0 + 32), columns [n0, n_end), the 32-column chunks half, half + kEpiHalves,
-// ...). Accumulator 0 (gate, TMEM columns [0, BN)) is read first, rounded to bf16, kept
-// in registers and stored; then, if `release0` is set, this warp's arrival on it lets
-// the MMA warp start the next tile's gate segment while accumulator 1 (up, columns
-// [BN, 2 BN)) is read and up and h = silu(gate) * up are stored.
+// ...). Accumulator 0 (gate, TMEM columns [0, BN)) is read first and kept in registers
+// as bf16; then, if `release0` is set, this warp's arrival on it lets the MMA warp start
+// the next tile's gate segment while accumulator 1 (up, columns [BN, 2 BN)) is read and
+// gate, up and h = silu(gate) * up are stored chunk by chunk.
 template <int BN, int CG, int kSlots, bool kTma>
 __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0, int32_t n0,
                                                int32_t n_end, uint32_t t_row,
@@ -622,8 +672,6 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 16; ++i) gk[j][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-      store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 0,
-                       y0 + col0, p.ldo, rows_valid, n_end - col0);
     }
   }
   if (release0 != nullptr) {
@@ -648,6 +696,8 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
         hk[i] = pack_bf16x2(swiglu_h(bf16_lo(gk[j][i]), bf16_lo(uk[i])),
                             swiglu_h(bf16_hi(gk[j][i]), bf16_hi(uk[i])));
       }
+      store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 0,
+                       y0 + col0, p.ldo, rows_valid, n_end - col0);
       store_chunk_bf16(ring, lane, uk, &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 1,
                        y1 + col0, p.ldo, rows_valid, n_end - col0);
       store_chunk_bf16(ring, lane, hk, &p.tmO[1], (p.tma_out & 2) != 0, col0, row0, 0,
@@ -671,7 +721,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint64_t* tfull_bar = empty_bar + Cfg::kStages;
   uint64_t* tempty_bar = tfull_bar + Cfg::kAccStages;
   uint64_t* done_bar = tempty_bar + Cfg::kTemptyBars;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* ld_bar = done_bar + 1;                   // kLdBars: the epilogue loaders'
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ld_bar + Cfg::kLdBars);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -695,7 +746,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int s = 0; s < Cfg::kTemptyBars; ++s)
       mbar_init(&tempty_bar[s], kEpiWarps * CG);   // one arrival per epilogue warp of the pair
     mbar_init(done_bar, 1);
+    for (int s = 0; s < Cfg::kLdBars; ++s) mbar_init(&ld_bar[s], 1);
     fence_barrier_init();
+  }
+  if (warp == 2 && lane == 0 && Cfg::kEpiStreams > 0 && p.tma_in) {
+    for (int t = 0; t < Cfg::kEpiStreams; ++t) tma_prefetch_desc(&p.tmE[t]);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA[0]);
@@ -894,6 +949,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int half = (warp - 2) / 4;           // which alternate column chunks it takes
     uint8_t* stg = smem + Cfg::kStgOffset + (warp - 2) * Cfg::kWarpStg;
     StoreRing<Cfg::kStoreSlots, Cfg::kTmaStore> ring{stg + Cfg::kLoadBytes, 0};
+    constexpr int kStreams = Cfg::kEpiStreams > 0 ? Cfg::kEpiStreams : 1;
+    using Loader = typename std::conditional<
+        (Cfg::kEpiStreams > 0),
+        EpiLoader<BN, Cfg::kTileN, Cfg::kTileM, kStreams, Cfg::kEpiDepth>, NoLoader>::type;
+    Loader ld{};
+    if constexpr (Cfg::kEpiStreams > 0) {
+      ld.p = &p;
+      ld.slots = stg;
+      ld.bars = ld_bar + (warp - 2) * Cfg::kEpiDepth;
+      ld.tile = first_tile;
+      ld.tile_stride = tile_stride;
+      ld.num_tiles = p.tma_in ? num_tiles : 0;
+      ld.j = 0;
+      ld.row_off = static_cast<int32_t>(pm) * (kBM * CG) + static_cast<int32_t>(rank) * kBM + q * 32;
+      ld.col_off = static_cast<int32_t>(pn) * BN;
+      ld.half = half;
+      ld.issued = 0;
+      ld.consumed = 0;
+    }
+    ld.start(lane);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
@@ -913,7 +988,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             Cfg::kSplitRelease ? &tempty_bar[0] : nullptr, leader_rank);
       } else {
         epilogue_tile<BN, MODE, Cfg::kStoreSlots, Cfg::kTmaStore>(
-            p, tc, row0, pn0, pend, t_row, stg, ring, lane,
+            p, tc, row0, pn0, pend, t_row, stg, ring, ld, lane,
             tc.n_blk * MCN + static_cast<int32_t>(pn), half);
       }
       tc_fence_before();
@@ -928,6 +1003,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    ld.drain();
     // this warp's TMA stores have read their slots and written global memory
     if constexpr (Cfg::kTmaStore) {
       if (lane == 0) bulk_wait_group<0>();
