@@ -127,11 +127,11 @@ struct GemmCfg {
   // through the warp's staging block measured faster.
   static constexpr bool kTmaStore = (MODE == EPI_GLU || MODE == EPI_UPGLU);
   // Epilogue inputs streamed by TMA (EpiLoader): gate and up for EPI_GLU, x for EPI_DX,
-  // kEpiDepth chunks ahead of the consumer.
+  // kEpiDepth chunks ahead of the consumer. One chunk ahead measured faster than two:
+  // the shared memory a second slot takes costs the mainloop a pipeline stage, and these
+  // short-K GEMMs with heavy epilogue traffic need the deeper operand pipeline more.
   static constexpr int kEpiStreams = (MODE == EPI_GLU) ? 2 : (MODE == EPI_DX ? 1 : 0);
-  // (one chunk ahead where two would leave the mainloop fewer than three stages: the
-  // single-CTA 256-wide tile with two streams)
-  static constexpr int kEpiDepth = (kEpiStreams == 2 && kStageBytes >= 48 * 1024) ? 1 : 2;
+  static constexpr int kEpiDepth = 1;
   // Staging per warp: load slots (the loader's kEpiDepth x kEpiStreams 2 KB slots, or one
   // 2 KB slot for EPI_DA's synchronous loads), then the store slots (2 KB each); fp32
   // partials use one 4 KB block.
