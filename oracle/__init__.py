@@ -29,6 +29,8 @@ from .bottleneck import (  # noqa: F401
     group_bounds,
     exchange_elems,
     rmsnorm_stats,
+    btp_shard_partials,
+    btp_reduce,
     block_fwd_reference,
     block_bwd_reference,
     block_fwd,

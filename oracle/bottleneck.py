@@ -172,6 +172,60 @@ def rmsnorm_stats(x, S, eps):
 
 
 # ---------------------------------------------------------------------------
+# The bottleneck-aware TP exchange (§2.1, with the statistics fused in per
+# §2.2), written out for S ranks on one host: what each rank sends, and the
+# reduction that replaces the all-reduce.
+# ---------------------------------------------------------------------------
+
+def btp_shard_partials(x, gamma, A, S, *, has_norm=True, flow="bf16"):
+    """What each of S tensor-parallel ranks contributes to the exchange.
+
+    Rank s holds columns [shard s] of x and rows [shard s] of the folded weight
+    A' (the down-projection is row-parallel, §2.1). It forms the unscaled
+    partial product x[:, shard s] @ A'[shard s, :] and, for a normed block, its
+    shard's per-row sums of squares (Online-RMSNorm, §2.2).
+    Returns (zpart [S, T, k*r], ssq [S, T] or None).
+    """
+    R = _round_fn(flow)
+    x = R(x)
+    A = R(A)
+    T, d = x.shape
+    off = shard_bounds(d, S)
+    Ap = R(R(gamma)[:, None] * A) if has_norm else A
+    zpart = np.empty((S, T, A.shape[1]))
+    ssq = np.empty((S, T)) if has_norm else None
+    for s in range(S):
+        xs = x[:, off[s]:off[s + 1]]
+        zpart[s] = xs @ Ap[off[s]:off[s + 1], :]
+        if has_norm:
+            ssq[s] = np.sum(xs * xs, axis=1)
+    return zpart, ssq
+
+
+def btp_reduce(zpart, ssq, d, *, act="silu", eps=1e-5, flow="bf16"):
+    """The exchange's reduction and the deferred normalisation after it.
+
+    Sums the partial products and the sums of squares over the ranks (shard
+    order), forms the row scale s from the full-d mean, and applies it and the
+    activation: z = s * sum_s zpart[s], a = act(z). Returns (a, s).
+    """
+    R = _round_fn(flow)
+    f, _ = act_fns[act]
+    S, T, _ = zpart.shape
+    zsum = np.zeros(zpart.shape[1:])
+    for s in range(S):
+        zsum = zsum + zpart[s]
+    if ssq is not None:
+        total = np.zeros(T)
+        for s in range(S):
+            total = total + ssq[s]
+        srow = 1.0 / np.sqrt(total / d + eps)
+    else:
+        srow = np.ones(T)
+    return R(f(srow[:, None] * zsum)), srow
+
+
+# ---------------------------------------------------------------------------
 # Plain definition (no sharding, no deferral, no grouping, no rounding).
 # ---------------------------------------------------------------------------
 
