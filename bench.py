@@ -300,12 +300,64 @@ def ours_arm(args, rank, world, local_rank):
 
     e2e_s = float("nan") if args.skip_aux else _e2e(args, mlp, w, x, dout, T, d, barrier,
                                                     dist, dev)
+    btp = None if args.skip_aux or rank != 0 else _btp_exchange(mlp, x, T, d, r, ffn, S)
     bi = 2 * T * d * 2          # x and dout, bf16
     bo = 2 * T * d * 2          # out and dx, bf16
     if rank != 0:
         return 0
     return _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r,
-                   ffn, S)
+                   ffn, S, btp)
+
+
+def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
+    """The bottleneck-aware TP exchange emulated on this GPU (outside the timed step):
+    per block, the S shards' partial products and sums of squares materialised as the
+    payload S ranks would all-reduce, then reduced; against what vanilla low-rank TP
+    all-reduces (each low-rank pair's d-wide output). Times are this GPU's cost of
+    forming and reducing the payload, not a network's."""
+    import torch
+
+    from rank_bottleneck_online_gb300 import binding as B
+
+    blocks = []
+    S_dn = 4   # the down block's d = ffn = 11008 splits into 64-aligned shards for S = 4
+    for name, blk, inp, s_blk in (("gate_up", mlp.gu, x, S), ("down", mlp.dn, mlp.h, S_dn)):
+        desc = B.make_desc(T, blk.desc.d, r, blk.desc.k, blk.desc.n, S=s_blk,
+                           has_norm=bool(blk.desc.has_norm))
+        ws = B.Workspace(B.workspace_bytes(desc))
+        pay = torch.empty(B.btp_payload_elems(desc), dtype=torch.float32, device=x.device)
+        y = torch.empty_like(blk.y)
+
+        def once():
+            B.block_fwd_btp(desc, inp, blk.gamma, blk.A, blk.B, ws, y=y, payload=pay)
+            B.block_fwd(desc, inp, blk.gamma, blk.A, blk.B, ws, y=y)
+
+        once()
+        torch.cuda.synchronize()
+        B.profile_enable(True)
+        for _ in range(reps):
+            once()
+        torch.cuda.synchronize()
+        pr = B.profile_read()
+        B.profile_enable(False)
+        B.check(ws)
+        kr = blk.desc.k * r
+        pay_rank = T * (kr + (1 if desc.has_norm else 0))
+        dwide_rank = T * blk.desc.k * blk.desc.n
+        part, red, fused = pr["gemm_down_partials"], pr["btp_exchange_reduce"], pr["gemm_down_act"]
+        blocks.append({
+            "block": name, "S": s_blk, "payload_elems_per_rank": pay_rank,
+            "vanilla_elems_per_rank": dwide_rank, "ratio": dwide_rank / pay_rank,
+            "ms_partials": part[1] / reps, "partials_tflops": part[2] / (part[1] / 1e3) / 1e12,
+            "ms_reduce": red[1] / reps, "reduce_gbs": red[3] / (red[1] / 1e3) / 1e9,
+            "ms_fused_down": fused[1] / reps})
+        del ws, pay
+    tot_pay = sum(b["payload_elems_per_rank"] for b in blocks)
+    tot_van = sum(b["vanilla_elems_per_rank"] for b in blocks)
+    return {"blocks": blocks, "mlp_ratio": tot_van / tot_pay,
+            "reading": "payload per rank: the bottleneck partials [T, k*r] (+1 column of "
+                       "sums of squares for a normed block); vanilla low-rank TP: one "
+                       "all-reduce of each low-rank pair's d-wide output ([T, k*n])"}
 
 
 def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
@@ -338,7 +390,7 @@ def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
 
 
 def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn,
-            S):
+            S, btp=None):
     ms_step = ms_total / args.steps
     tokens_per_s = aggregate_rate(world, T * args.steps, ms_total / 1e3)
     exe, model = mlp_flops(T, d, r, ffn)
@@ -408,6 +460,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "btp_exchange": btp,
     }
     print(json.dumps(line), flush=True)
     return 0

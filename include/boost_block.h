@@ -201,6 +201,34 @@ boost_status boost_rmsnorm_rstd_noalloc(const boost_block_desc* desc, const void
                                         float* rstd, void* stream);
 
 /*
+ * Forward of one block with the down-projection run as an explicit emulation of
+ * the bottleneck-aware tensor-parallel exchange (technical summary §2.1: the
+ * down-projection is row-parallel over d, and one all-reduce of the narrow [T, k*r]
+ * activations replaces one of d-wide ones; §2.2: the Online-RMSNorm statistics ride
+ * on the same exchange). The S column shards of d stand for S ranks:
+ *   1. per shard s, the unscaled partial product x[:, shard s] @ A'[shard s, :]
+ *      (one split-K tensor-core GEMM whose splits are the shards) and, for a normed
+ *      block, the shard's per-row sums of squares: the payload each rank sends;
+ *   2. the reduction over the shards in shard order (standing in for the
+ *      all-reduce), the row scale from the summed sums of squares (full-d mean) and
+ *      a = act(s * z);
+ *   3. the batched up-projection, as in boost_block_fwd.
+ * Arguments as boost_block_fwd, plus
+ *   payload  device fp32 [S*T*k*r + has_norm*S*T], caller-owned, written: the
+ *            partial products [S, T, k*r], then (normed blocks) the sums of squares
+ *            [S, T]; the values S ranks would contribute to the exchange.
+ * y equals boost_block_fwd's up to fp32 summation order (the shard partials are
+ * summed after rounding to fp32). Requires d % S == 0 and d / S a multiple of 64
+ * (whole k-blocks per shard), else BOOST_ERR_UNSUPPORTED_SHAPE. The fused path
+ * (boost_block_fwd) computes the same block without materialising the payload; this
+ * entry exists to measure the exchange the pages' design performs.
+ */
+boost_status boost_block_fwd_btp(const boost_block_desc* desc,
+                                 const void* x, const void* gamma, const void* A, const void* B,
+                                 void* y, float* rstd, float* payload,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Exact bookkeeping of the shard and group partition (host only, no CUDA).
  *   shard_off       host [S+1]: shard s covers columns [shard_off[s], shard_off[s+1]) of d
  *   group_col_off   host [k+1]: group i covers columns [off[i], off[i+1]) of A

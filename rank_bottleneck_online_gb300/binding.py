@@ -32,7 +32,7 @@ EXPORTS = (
     "boost_swiglu_fwd", "boost_swiglu_bwd", "boost_add", "boost_debug_wait_timeout",
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
-    "boost_profile_read_kernels", "boost_block_fwd_swiglu",
+    "boost_profile_read_kernels", "boost_block_fwd_swiglu", "boost_block_fwd_btp",
 )
 
 
@@ -71,6 +71,7 @@ def lib():
     L.boost_block_ws_init.argtypes = [vp, sz, vp]
     L.boost_block_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_fwd_swiglu.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.boost_block_fwd_btp.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_rmsnorm_stats.argtypes = [dp, vp, vp, vp, vp]
     L.boost_block_layout.argtypes = [dp, ctypes.POINTER(i64), ctypes.POINTER(i64),
@@ -253,6 +254,42 @@ def block_fwd_swiglu(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, h=Non
                                         _stream(stream)),
            "boost_block_fwd_swiglu")
     return y, h
+
+
+def btp_payload_elems(desc: Desc) -> int:
+    """fp32 values of the emulated exchange payload: S*T*k*r partial products, then
+    (normed blocks) S*T sums of squares."""
+    return desc.S * desc.T * (desc.k * desc.r + (1 if desc.has_norm else 0))
+
+
+def block_fwd_btp(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=None,
+                  payload=None, stream=None):
+    """Forward with the down-projection as the emulated bottleneck-aware TP exchange.
+    Returns (y [k,T,n], zpart [S,T,k*r], ssq [S,T] or None), the last two views of the
+    payload buffer."""
+    bf = torch.bfloat16
+    _need(x, "x", bf, (desc.T, desc.d))
+    _need(A, "A", bf, (desc.d, desc.k * desc.r))
+    _need(B, "B", bf, (desc.k, desc.r, desc.n))
+    if desc.has_norm:
+        _need(gamma, "gamma", bf, (desc.d,))
+    if y is None:
+        y = torch.empty(desc.k, desc.T, desc.n, dtype=bf, device=x.device)
+    _need(y, "y", bf, (desc.k, desc.T, desc.n))
+    n_pay = btp_payload_elems(desc)
+    if payload is None:
+        payload = torch.empty(n_pay, dtype=torch.float32, device=x.device)
+    _need(payload, "payload", torch.float32, (n_pay,))
+    if rstd is not None:
+        _need(rstd, "rstd", torch.float32, (desc.T,))
+    _check(lib().boost_block_fwd_btp(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(A), _ptr(B),
+                                     _ptr(y), _ptr(rstd), _ptr(payload), ws.ptr, ws.nbytes,
+                                     _stream(stream)),
+           "boost_block_fwd_btp")
+    S, T, kr = desc.S, desc.T, desc.k * desc.r
+    zpart = payload[:S * T * kr].view(S, T, kr)
+    ssq = payload[S * T * kr:].view(S, T) if desc.has_norm else None
+    return y, zpart, ssq
 
 
 def block_bwd(desc: Desc, x, gamma, A, B, dy, ws: Workspace, *, rstd=None, dx=None,

@@ -482,12 +482,15 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x, fl
 
 namespace {
 
-// Forward of one block. With `h` non-NULL (k == 2: gate and up groups) the up-projection
+// Forward of one block. With `glu` (k == 2: gate and up groups) the up-projection
 // computes both groups of a tile in one kernel and its epilogue also writes
-// h = silu(gate) * up.
+// h = silu(gate) * up. With `payload` non-NULL the down-projection runs as the explicit
+// emulation of the bottleneck-aware TP exchange: per-shard partial products and sums
+// of squares into the payload, then the reduction that stands in for the all-reduce.
 boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const void* gamma,
                             const void* A, const void* B, void* y, void* h, bool glu,
-                            float* rstd, void* ws, size_t ws_bytes, void* stream) {
+                            float* rstd, float* payload, bool btp, void* ws, size_t ws_bytes,
+                            void* stream) {
   boost_status st = validate_desc(desc);
   if (st != BOOST_OK) return st;
   const boost_block_desc& D = *desc;
@@ -499,6 +502,12 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
   if (st != BOOST_OK) return st;
   if (glu && D.T > 0 && h == nullptr) return BOOST_ERR_INVALID_ARG;
   if (D.has_norm && gamma == nullptr) return BOOST_ERR_INVALID_ARG;
+  if (btp) {
+    // every shard is a whole number of the GEMM's 64-deep k-blocks
+    if (D.d % D.S != 0 || (D.d / D.S) % kBK != 0) return BOOST_ERR_UNSUPPORTED_SHAPE;
+    if (D.T > 0 && payload == nullptr) return BOOST_ERR_INVALID_ARG;
+    if (payload != nullptr && !aligned16(payload)) return BOOST_ERR_ALIGNMENT;
+  }
   const int sms = current_num_sms();
   const Plan P = make_plan(D, sms);
   st = check_ws(ws, ws_bytes, P.total);
@@ -509,12 +518,18 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
 
   const void* Ap = A;
   float* rs = nullptr;
+  float* zpart = payload;                                   // [S, T, kr]
+  float* ssq_x = btp && D.has_norm ? payload + D.S * D.T * P.kr : nullptr;   // [S, T]
   if (D.has_norm) {
     rs = rstd ? rstd : ws_at<float>(ws, P.off_rstd);
     cudaError_t e;
     {
+      // (under the emulated exchange the shard sums of squares go into the payload; the
+      // row scale is formed again after the reduction, from the exchanged sums)
       ProfScope ps(s, K_STATS, 0.0, stats_bytes(P, D.S));
-      e = launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq), rs, s);
+      e = launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps,
+                               btp ? ssq_x : ws_at<float>(ws, P.off_ssq),
+                               btp ? ws_at<float>(ws, P.off_rstd) : rs, s);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
     {
@@ -526,18 +541,39 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
   }
   void* a = ws_at<void>(ws, P.off_a);
 
-  // K2: a = act(s * (x @ A')) over all k groups in one GEMM.
   GemmParams g = base_params(P, err);
   if (!down_segment(g, P, x, Ap, P.down, P.tpg_down)) return BOOST_ERR_CUDA;
-  g.act = D.act;
-  g.rstd = rs;
-  g.out = a;
-  g.ldo = P.kr;
   cudaError_t e;
-  {
+  if (!btp) {
+    // K2: a = act(s * (x @ A')) over all k groups in one GEMM.
+    g.act = D.act;
+    g.rstd = rs;
+    g.out = a;
+    g.ldo = P.kr;
     ProfScope ps(s, K_DOWN, 2.0 * P.T * P.d * P.kr,
                  2.0 * (P.T * P.d + P.d * P.kr + P.T * P.kr) + 4.0 * P.T);
     e = launch_gemm_rows(P.down, EPI_ACT, g, sms, s);
+  } else {
+    // Each shard's unscaled partial product x[:, shard] @ A'[shard, :] (a split-K GEMM
+    // whose splits are the shards), then the reduction over the shards that stands in
+    // for the all-reduce, with the deferred row scale and the activation after it.
+    g.splits = D.S;
+    g.kb_per_split = static_cast<int32_t>(D.d / D.S / kBK);
+    g.out = zpart;
+    g.ldo = P.kr;
+    g.out_sstride = D.T * P.kr;
+    {
+      ProfScope ps(s, K_BTP_PARTIAL, 2.0 * P.T * P.d * P.kr,
+                   2.0 * (P.T * P.d + P.d * P.kr) + 4.0 * D.S * P.T * P.kr);
+      e = launch_gemm_rows(P.down, EPI_F32, g, sms, s);
+    }
+    if (e == cudaSuccess) {
+      ProfScope ps(s, K_BTP_REDUCE, 0.0,
+                   4.0 * D.S * P.T * (P.kr + (D.has_norm ? 1 : 0)) + 2.0 * P.T * P.kr +
+                       (D.has_norm ? 4.0 * P.T : 0.0));
+      e = launch_btp_reduce(zpart, ssq_x, static_cast<int>(D.S), D.T, P.kr, D.d, D.eps, D.act, a,
+                            D.has_norm ? rs : nullptr, s);
+    }
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
@@ -587,14 +623,23 @@ extern "C" {
 boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const void* gamma,
                              const void* A, const void* B, void* y, float* rstd, void* ws,
                              size_t ws_bytes, void* stream) {
-  return block_fwd_impl(desc, x, gamma, A, B, y, nullptr, false, rstd, ws, ws_bytes, stream);
+  return block_fwd_impl(desc, x, gamma, A, B, y, nullptr, false, rstd, nullptr, false, ws,
+                        ws_bytes, stream);
+}
+
+boost_status boost_block_fwd_btp(const boost_block_desc* desc, const void* x, const void* gamma,
+                                 const void* A, const void* B, void* y, float* rstd,
+                                 float* payload, void* ws, size_t ws_bytes, void* stream) {
+  return block_fwd_impl(desc, x, gamma, A, B, y, nullptr, false, rstd, payload, true, ws,
+                        ws_bytes, stream);
 }
 
 boost_status boost_block_fwd_swiglu(const boost_block_desc* desc, const void* x,
                                     const void* gamma, const void* A, const void* B, void* y,
                                     void* h, float* rstd, void* ws, size_t ws_bytes,
                                     void* stream) {
-  return block_fwd_impl(desc, x, gamma, A, B, y, h, true, rstd, ws, ws_bytes, stream);
+  return block_fwd_impl(desc, x, gamma, A, B, y, h, true, rstd, nullptr, false, ws, ws_bytes,
+                        stream);
 }
 
 }  // extern "C"

@@ -24,6 +24,9 @@ cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, flo
                                  float* ssq, float* rstd, cudaStream_t stream);
 cudaError_t launch_fold_gamma(const void* gamma, const void* A, void* Ap, int64_t d, int64_t kr,
                               cudaStream_t stream);
+cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64_t T,
+                              int64_t kr, int64_t d, float eps, int act, void* a, float* rstd,
+                              cudaStream_t stream);
 cudaError_t launch_swiglu_fwd(const void* g, const void* u, void* h, int64_t count,
                               cudaStream_t stream);
 cudaError_t launch_swiglu_bwd(const void* g, const void* u, const void* dh, void* dg, void* du,

@@ -93,6 +93,43 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
   if (lane == 0) rstd[row] = 1.0f / sqrtf(total / static_cast<float>(d) + eps);
 }
 
+// The reduction standing in for the bottleneck-aware TP all-reduce (BOOST technical
+// summary §2.1, statistics fused per §2.2): z = sum over shards of the partial products
+// zpart [S, T, kr] (shard order), the row scale from the summed sums of squares
+// ssq [S, T] (full-d mean, the same expression and order as rmsnorm_stats_kernel), and
+// a = bf16(act(s * z)) with the GEMM epilogue's activation. One thread per 8 columns.
+__global__ void __launch_bounds__(kThreads) btp_reduce_kernel(
+    const float* __restrict__ zpart, const float* __restrict__ ssq, int S, int64_t T,
+    int64_t kr, int64_t d, float eps, int act, uint4* __restrict__ a, float* __restrict__ rstd) {
+  const int64_t nv = kr / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < T * nv;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t t = i / nv;
+    const int64_t v = i - t * nv;
+    float srow = 1.0f;
+    if (ssq != nullptr) {
+      float total = 0.0f;
+      for (int s = 0; s < S; ++s) total += ssq[static_cast<int64_t>(s) * T + t];
+      srow = 1.0f / sqrtf(total / static_cast<float>(d) + eps);
+      if (v == 0 && rstd != nullptr) rstd[t] = srow;
+    }
+    float z[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    for (int s = 0; s < S; ++s) {
+      const float4* src =
+          reinterpret_cast<const float4*>(zpart + (static_cast<int64_t>(s) * T + t) * kr) + 2 * v;
+      const float4 p0 = src[0], p1 = src[1];
+      z[0] += p0.x; z[1] += p0.y; z[2] += p0.z; z[3] += p0.w;
+      z[4] += p1.x; z[5] += p1.y; z[6] += p1.z; z[7] += p1.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float f = srow * z[e];
+      z[e] = act == 1 ? silu_f(f) : f;
+    }
+    a[i] = pack8(z);
+  }
+}
+
 // A'[j, m] = bf16(gamma_j * A[j, m]); the product of two bf16 values is exact in fp32.
 __global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
     const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
@@ -267,6 +304,15 @@ cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, flo
   const int64_t grid = (T + rows_per_block - 1) / rows_per_block;
   rmsnorm_stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64_t T,
+                              int64_t kr, int64_t d, float eps, int act, void* a, float* rstd,
+                              cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  btp_reduce_kernel<<<grid_for(T * (kr / 8), kThreads), kThreads, 0, stream>>>(
+      zpart, ssq, S, T, kr, d, eps, act, static_cast<uint4*>(a), rstd);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ enum KernelId : int {
   K_PROBE,
   K_DX_GLU,
   K_UP_GLU,
+  K_BTP_PARTIAL,
+  K_BTP_REDUCE,
   K_COUNT
 };
 

@@ -142,6 +142,21 @@ def test_fused_swiglu_forward_argument_checks(L):
     assert fwd_glu(B.make_desc(128, 256, 64, 2, 256, S=4), f(0x6008)) == 3   # h misaligned
 
 
+def test_btp_emulation_argument_checks(L):
+    f = _fake
+
+    def fwd_btp(desc, payload):
+        return L.boost_block_fwd_btp(ctypes.byref(desc), f(0x1000), f(0x2000), f(0x3000),
+                                     f(0x4000), f(0x5000), None, payload, f(0x100000), 1 << 30,
+                                     None)
+
+    # shards must be whole 64-deep k-blocks: d / S = 48
+    assert fwd_btp(B.make_desc(128, 192, 64, 2, 256, S=4), f(0x6000)) == 2
+    assert fwd_btp(B.make_desc(128, 256, 64, 2, 256, S=4), None) == 1       # payload missing
+    assert fwd_btp(B.make_desc(128, 256, 64, 2, 256, S=4), f(0x6004)) == 3  # misaligned
+    assert fwd_btp(B.make_desc(128, 256, 64, 2, 256, S=3), f(0x6000)) == 2  # d % S != 0
+
+
 def test_elementwise_argument_checks(L):
     assert L.boost_swiglu_fwd(4, 12, _fake(0x1000), _fake(0x2000), _fake(0x3000), None) == 2
     assert L.boost_swiglu_fwd(-1, 8, _fake(0x1000), _fake(0x2000), _fake(0x3000), None) == 1
