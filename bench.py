@@ -44,6 +44,70 @@ def mlp_flops(T, d, r, ffn):
     return exe, model
 
 
+def dense_mlp_flops(T, d, ffn):
+    """Dense (full-rank) LLaMA MLP fwd + bwd: three [d, ffn]-sized GEMMs, each 2 flops per
+    multiply-add, forward once and twice in backward (dgrad and wgrad)."""
+    return 6.0 * T * 3 * d * ffn
+
+
+def dense_mlp(T, d, ffn, device, seed=0, dtype=None, eps=1e-5):
+    """The full-rank counterpart of the low-rank MLP at the same shapes, in plain torch
+    (cuBLAS GEMMs, torch's RMSNorm and SiLU): out = (silu(n @ Wg) * (n @ Wu)) @ Wd with
+    n = RMSNorm(x) * gamma. Context for the low-rank step, not part of the library.
+    Returns (step, tensors); step() runs forward and backward once."""
+    import torch
+    import torch.nn.functional as F
+
+    dtype = dtype or torch.bfloat16
+    g = torch.Generator(device="cpu").manual_seed(seed)
+
+    def randn(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g) * std).to(dtype).to(device)
+
+    t = {"x": randn(T, d), "gamma": (1.0 + 0.1 * torch.randn(d, generator=g)).to(dtype).to(device),
+         "Wg": randn(d, ffn, std=d ** -0.5), "Wu": randn(d, ffn, std=d ** -0.5),
+         "Wd": randn(ffn, d, std=ffn ** -0.5), "dout": randn(T, d)}
+    for k in ("x", "gamma", "Wg", "Wu", "Wd"):
+        t[k].requires_grad_(True)
+
+    def step():
+        for k in ("x", "gamma", "Wg", "Wu", "Wd"):
+            t[k].grad = None
+        n = F.rms_norm(t["x"], (d,), t["gamma"], eps)
+        h = F.silu(n @ t["Wg"]) * (n @ t["Wu"])
+        out = h @ t["Wd"]
+        out.backward(t["dout"])
+        return out
+
+    return step, t
+
+
+def _dense_context(T, d, ffn, ms_ours, reps=10):
+    """Time the full-rank MLP step on this GPU (CUDA events, after warm-up) against the
+    low-rank step's ms_per_step: the one-GPU analogue of the pages' full-rank vs
+    low-rank comparison."""
+    import torch
+
+    step, t = dense_mlp(T, d, ffn, "cuda")
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del t, step
+    torch.cuda.empty_cache()
+    fl = dense_mlp_flops(T, d, ffn)
+    return {"impl": "torch eager, cuBLAS bf16 GEMMs", "ms_per_step": ms,
+            "tokens_per_s": T / (ms / 1e3), "tflops_per_s": fl / (ms / 1e3) / 1e12,
+            "flops_per_step": fl, "lowrank_speedup": ms / ms_ours}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -301,12 +365,14 @@ def ours_arm(args, rank, world, local_rank):
     e2e_s = float("nan") if args.skip_aux else _e2e(args, mlp, w, x, dout, T, d, barrier,
                                                     dist, dev)
     btp = None if args.skip_aux or rank != 0 else _btp_exchange(mlp, x, T, d, r, ffn, S)
+    dense = (None if args.skip_aux or rank != 0
+             else _dense_context(T, d, ffn, ms_total / args.steps))
     bi = 2 * T * d * 2          # x and dout, bf16
     bo = 2 * T * d * 2          # out and dx, bf16
     if rank != 0:
         return 0
     return _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r,
-                   ffn, S, btp)
+                   ffn, S, btp, dense)
 
 
 def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
@@ -362,35 +428,63 @@ def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
 
 def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
     """Seconds for args.steps steps through the public API from pinned host buffers:
-    each step copies x and dout in, runs forward + backward, copies out and dx back."""
+    each step copies its x and dout in, runs forward + backward and copies out and dx
+    back. The copies are pipelined against the compute on two more streams (inputs of
+    step i+1 in, results of step i-1 out, while step i computes) with double-buffered
+    device tensors; every step's copies lie inside the timed region."""
     import torch
 
+    from rank_bottleneck_online_gb300.block import MLP
+
+    c = _cfg()
+    r, ffn, S = c["r"], c["ffn"], c["S"]
     x_h = w["x"].pin_memory()
     dout_h = w["dout"].pin_memory()
-    out_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
-    dx_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+    out_h = [torch.empty(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dx_h = [torch.empty(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    # a second replica of the MLP (same weights) so that step i+1 does not overwrite the
+    # results step i is still copying out
+    mlps = [mlp, MLP(T, d, r, ffn, S=S, weights=w, device=dev)]
+    xs = [x, torch.empty_like(x)]
+    douts = [dout, torch.empty_like(dout)]
+    comp = torch.cuda.current_stream()
+    h2d = torch.cuda.Stream()
+    d2h = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()   # noqa: E731
+    in_ready = [ev(), ev()]
+    computed = [ev(), ev()]
+    copied_out = [ev(), ev()]
 
-    def e2e_step():
-        x.copy_(x_h, non_blocking=True)
-        dout.copy_(dout_h, non_blocking=True)
-        mlp.forward(x)
-        mlp.backward(x, dout)
-        out_h.copy_(mlp.out, non_blocking=True)
-        dx_h.copy_(mlp.gu.dx, non_blocking=True)
+    def run(n):
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(computed[b])          # step i-2 finished with these inputs
+                xs[b].copy_(x_h, non_blocking=True)
+                douts[b].copy_(dout_h, non_blocking=True)
+                in_ready[b].record(h2d)
+            comp.wait_event(in_ready[b])
+            comp.wait_event(copied_out[b])            # step i-2's results are out
+            mlps[b].forward(xs[b])
+            mlps[b].backward(xs[b], douts[b])
+            computed[b].record(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(computed[b])
+                out_h[b].copy_(mlps[b].out, non_blocking=True)
+                dx_h[b].copy_(mlps[b].gu.dx, non_blocking=True)
+                copied_out[b].record(d2h)
 
-    for _ in range(2):
-        e2e_step()
+    run(2)
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
+    run(args.steps)
     torch.cuda.synchronize()
     return max_over_ranks(time.perf_counter() - t0, dist, dev)
 
 
 def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn,
-            S, btp=None):
+            S, btp=None, dense=None):
     ms_step = ms_total / args.steps
     tokens_per_s = aggregate_rate(world, T * args.steps, ms_total / 1e3)
     exe, model = mlp_flops(T, d, r, ffn)
@@ -461,6 +555,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "btp_exchange": btp,
+        "dense_fullrank": dense,
     }
     print(json.dumps(line), flush=True)
     return 0

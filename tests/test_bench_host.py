@@ -60,3 +60,35 @@ def test_reference_arm_nonzero_ranks_do_no_work(capsys):
         steps, warmup = 1, 0
     assert bench.reference_arm(A(), rank=1, world=2) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_dense_fullrank_context_is_the_textbook_mlp():
+    # the full-rank comparison leg (torch) against the plain fp64 definition on a tiny
+    # case: forward and every gradient
+    import numpy as np
+
+    T, d, ffn = 6, 16, 24
+    step, t = bench.dense_mlp(T, d, ffn, "cpu", seed=3, dtype=torch.float64)
+    out = step().detach().numpy()
+    x, g, Wg, Wu, Wd, dout = (t[k].detach().numpy() for k in ("x", "gamma", "Wg", "Wu", "Wd",
+                                                                 "dout"))
+    rs = 1.0 / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-5)
+    n = x * rs * g
+    a, b = n @ Wg, n @ Wu
+    sg = 1.0 / (1.0 + np.exp(-a))
+    h = a * sg * b
+    np.testing.assert_allclose(out, h @ Wd, rtol=1e-12, atol=1e-12)
+    dh = dout @ Wd.T
+    da = dh * b * sg * (1 + a * (1 - sg))
+    db = dh * a * sg
+    dn = da @ Wg.T + db @ Wu.T
+    np.testing.assert_allclose(t["Wd"].grad.numpy(), h.T @ dout, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(t["Wg"].grad.numpy(), n.T @ da, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(t["Wu"].grad.numpy(), n.T @ db, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(t["gamma"].grad.numpy(), (dn * x * rs).sum(axis=0), rtol=1e-10,
+                               atol=1e-12)
+    xh = x * rs
+    dxh = dn * g
+    dx = rs * (dxh - xh * (dxh * xh).mean(axis=1, keepdims=True))
+    np.testing.assert_allclose(t["x"].grad.numpy(), dx, rtol=1e-10, atol=1e-12)
+    assert bench.dense_mlp_flops(T, d, ffn) == 6.0 * T * 3 * d * ffn
