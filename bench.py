@@ -108,6 +108,39 @@ def _dense_context(T, d, ffn, ms_ours, reps=10):
             "flops_per_step": fl, "lowrank_speedup": ms / ms_ours}
 
 
+def _checkpoint_cuts(mlp, w, x, dout, T, d, r, ffn, S, ms_input, reps=10):
+    """The step with the bottleneck checkpoint cut (only the gate/up block's r-wide
+    activation kept; gate, up and h regenerated in backward) against the timed step,
+    which keeps the blocks' inputs: time per step and bytes kept between forward and
+    backward beyond x and the row scale."""
+    import torch
+
+    from rank_bottleneck_online_gb300.block import MLP
+
+    m2 = MLP(T, d, r, ffn, S=S, weights=w, device=x.device, checkpoint="bottleneck")
+
+    def step():
+        m2.forward(x)
+        m2.backward(x, dout)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    out = {"input": {"ms_per_step": ms_input, "saved_bytes": mlp.saved_bytes()},
+           "bottleneck": {"ms_per_step": ms, "saved_bytes": m2.saved_bytes()}}
+    del m2
+    torch.cuda.empty_cache()
+    return out
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -367,12 +400,14 @@ def ours_arm(args, rank, world, local_rank):
     btp = None if args.skip_aux or rank != 0 else _btp_exchange(mlp, x, T, d, r, ffn, S)
     dense = (None if args.skip_aux or rank != 0
              else _dense_context(T, d, ffn, ms_total / args.steps))
+    cuts = (None if args.skip_aux or rank != 0
+            else _checkpoint_cuts(mlp, w, x, dout, T, d, r, ffn, S, ms_total / args.steps))
     bi = 2 * T * d * 2          # x and dout, bf16
     bo = 2 * T * d * 2          # out and dx, bf16
     if rank != 0:
         return 0
     return _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r,
-                   ffn, S, btp, dense)
+                   ffn, S, btp, dense, cuts)
 
 
 def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
@@ -484,7 +519,7 @@ def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
 
 
 def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn,
-            S, btp=None, dense=None):
+            S, btp=None, dense=None, cuts=None):
     ms_step = ms_total / args.steps
     tokens_per_s = aggregate_rate(world, T * args.steps, ms_total / 1e3)
     exe, model = mlp_flops(T, d, r, ffn)
@@ -556,6 +591,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
         "cpu_baseline": cpu,
         "btp_exchange": btp,
         "dense_fullrank": dense,
+        "checkpoint_cuts": cuts,
     }
     print(json.dumps(line), flush=True)
     return 0

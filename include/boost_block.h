@@ -201,6 +201,23 @@ boost_status boost_rmsnorm_rstd_noalloc(const boost_block_desc* desc, const void
                                         float* rstd, void* stream);
 
 /*
+ * The batched up-projection alone, from a caller-provided bottleneck activation:
+ * y[i] = a[:, group i] @ B[i]; with h non-NULL (k == 2: gate and up groups) the
+ * gate/up form of boost_block_fwd_swiglu, also writing h = silu(y[0]) * y[1]. For
+ * the checkpoint cut at the bottleneck (technical summary §2.2, low-rank activation
+ * checkpointing; §2.1 places the tensor-parallel block boundary at the r-wide
+ * activations): a caller that kept only a from the forward regenerates the d-wide
+ * section in backward. Bitwise equal to the up-projection inside the block forward.
+ *   a   [T, k*r]  bottleneck activation (the block forward's act(z))
+ *   B   [k, r, n] up-projection weights
+ *   y   [k, T, n] out
+ *   h   [T, n]    out, optional (NULL: plain up-projection)
+ *   ws  workspace as for boost_block_fwd (its error word is used)
+ */
+boost_status boost_block_up(const boost_block_desc* desc, const void* a, const void* B,
+                            void* y, void* h, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Forward of one block with the down-projection run as an explicit emulation of
  * the bottleneck-aware tensor-parallel exchange (technical summary §2.1: the
  * down-projection is row-parallel over d, and one all-reduce of the narrow [T, k*r]

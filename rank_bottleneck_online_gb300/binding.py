@@ -33,6 +33,7 @@ EXPORTS = (
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
     "boost_profile_read_kernels", "boost_block_fwd_swiglu", "boost_block_fwd_btp",
+    "boost_block_up",
 )
 
 
@@ -72,6 +73,7 @@ def lib():
     L.boost_block_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_fwd_swiglu.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_fwd_btp.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.boost_block_up.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_rmsnorm_stats.argtypes = [dp, vp, vp, vp, vp]
     L.boost_block_layout.argtypes = [dp, ctypes.POINTER(i64), ctypes.POINTER(i64),
@@ -254,6 +256,22 @@ def block_fwd_swiglu(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, h=Non
                                         _stream(stream)),
            "boost_block_fwd_swiglu")
     return y, h
+
+
+def block_up(desc: Desc, a, B, ws: Workspace, *, y=None, h=None, stream=None):
+    """The up-projection alone from a given bottleneck activation a [T, k*r]; with h
+    (k == 2) also h = silu(y[0]) * y[1]. Returns y (and h)."""
+    bf = torch.bfloat16
+    _need(a, "a", bf, (desc.T, desc.k * desc.r))
+    _need(B, "B", bf, (desc.k, desc.r, desc.n))
+    if y is None:
+        y = torch.empty(desc.k, desc.T, desc.n, dtype=bf, device=a.device)
+    _need(y, "y", bf, (desc.k, desc.T, desc.n))
+    if h is not None:
+        _need(h, "h", bf, (desc.T, desc.n))
+    _check(lib().boost_block_up(ctypes.byref(desc), _ptr(a), _ptr(B), _ptr(y), _ptr(h), ws.ptr,
+                                ws.nbytes, _stream(stream)), "boost_block_up")
+    return y if h is None else (y, h)
 
 
 def btp_payload_elems(desc: Desc) -> int:

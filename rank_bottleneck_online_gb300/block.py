@@ -54,19 +54,32 @@ class MLP:
     """LLaMA MLP of two bottlenecks: gate/up (normed, k=2) -> SwiGLU -> down (k=1)."""
 
     def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, act="silu", weights=None,
-                 device="cuda", ws=None, fused_glu=True):
+                 device="cuda", ws=None, fused_glu=True, checkpoint="input"):
         w = weights or {}
-        self.T, self.d, self.ffn = T, d, ffn
+        self.T, self.d, self.r, self.ffn = T, d, r, ffn
         # SwiGLU forward in the gate/up up-projection's epilogue, and its backward in the
         # down block's dgrad epilogue (False: separate SwiGLU passes)
         self.fused_glu = fused_glu
+        # What the backward starts from. "input": each block's input (x, and h with the
+        # gate/up values it was formed from) is kept from the forward, and each block
+        # regenerates its own bottleneck activation. "bottleneck": only the gate/up
+        # block's r-wide bottleneck activation is kept; the backward regenerates gate,
+        # up and h from it (the cut at the tensor-parallel block boundary of §2.1).
+        if checkpoint not in ("input", "bottleneck"):
+            raise ValueError("checkpoint is 'input' or 'bottleneck'")
+        if checkpoint == "bottleneck" and not fused_glu:
+            raise ValueError("the bottleneck cut regenerates gate, up and h with the fused kernel")
+        self.checkpoint = checkpoint
         self.gu = Block(T, d, r, 2, ffn, S=S, eps=eps, act=act, has_norm=True,
                         weights={"gamma": w.get("gamma"), "A": w.get("A1"), "B": w.get("B1")},
                         device=device, ws=ws)
         self.dn = Block(T, ffn, r, 1, d, S=1, eps=eps, act=act, has_norm=False,
                         weights={"A": w.get("A2"), "B": w.get("B2")}, device=device,
-                        ws=self.gu.ws)
-        self.gu.ws = self.dn.ws       # one workspace sized for both blocks
+                        ws=self.gu.ws if checkpoint == "input" else None)
+        if checkpoint == "input":
+            self.gu.ws = self.dn.ws   # one workspace sized for both blocks
+        # (bottleneck cut: the gate/up block keeps its own workspace, whose a survives
+        # the down block's forward)
         dev = self.gu.device
         self.h = torch.empty(T, ffn, dtype=torch.bfloat16, device=dev)
         self.dy1 = torch.empty(2, T, ffn, dtype=torch.bfloat16, device=dev)
@@ -85,8 +98,21 @@ class MLP:
             B.swiglu_fwd(y1[0], y1[1], self.h, stream=stream)
         return self.dn.forward(self.h, stream)[0]
 
+    def saved_bytes(self):
+        """Bytes of activations the backward needs from the forward beyond the input x
+        and the row scale: gate, up and h for the input cut, the gate/up block's
+        bottleneck activation for the bottleneck cut."""
+        if self.checkpoint == "input":
+            return 3 * self.T * self.ffn * 2
+        return self.T * 2 * self.r * 2
+
     def backward(self, x, dout, stream=None):
         dy2 = dout.view(1, self.T, self.d)
+        if self.checkpoint == "bottleneck":
+            gu = self.gu
+            a1 = B.ws_view(gu.ws, B.ws_layout(gu.desc)["a"], (self.T, 2 * self.r),
+                           torch.bfloat16)
+            B.block_up(gu.desc, a1, gu.B, gu.ws, y=gu.y, h=self.h, stream=stream)
         if self.fused_glu:
             B.block_bwd_swiglu(self.dn.desc, self.h, self.dn.A, self.dn.B, dy2, self.gu.y[0],
                                self.gu.y[1], self.dn.ws, dgate=self.dy1[0], dup=self.dy1[1],

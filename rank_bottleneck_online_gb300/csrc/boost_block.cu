@@ -482,6 +482,49 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x, fl
 
 namespace {
 
+// K3, the batched up-projection y[i] = a[:, group i] @ B[i]; with `glu` (k == 2) one
+// kernel computes both groups of a tile and also writes h = silu(y[0]) * y[1].
+cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void* h, bool glu,
+                      DeviceError* err, int sms, cudaStream_t s) {
+  cudaError_t e;
+  GemmParams u = base_params(P, err);
+  if (!make_map(&u.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, P.up.a_rows()))
+    return cudaErrorInvalidValue;   // a tensor map could not be encoded
+  if (!make_map(&u.tmB[0], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, 64, 1))
+    return cudaErrorInvalidValue;
+  u.seg[0].a = OperandView{2, 0, 1, 0};   // a as (r, k, T): K-major, batch = group
+  u.seg[0].b = OperandView{0, 1, 2, 1};   // B as (n, r, k): MN-major
+  u.seg[0].num_kb = static_cast<int32_t>(cdiv(P.r, kBK));
+  u.M = static_cast<int32_t>(P.T);
+  u.N = static_cast<int32_t>(P.n);
+  u.batch = static_cast<int32_t>(P.k);
+  u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.up.super_n()));
+  u.m_inner = 0;
+  u.out = y;
+  u.ldo = P.n;
+  u.out_bstride = P.T * P.n;
+  if (glu) {
+    // one tile list; segment 0 = the gate group into accumulator 0, segment 1 = the up
+    // group (same maps, batch index + 1) into accumulator 1
+    u.batch = 1;
+    u.num_seg = 2;
+    u.seg[1] = u.seg[0];
+    u.seg[1].batch_add = 1;
+    u.tmA[1] = u.tmA[0];
+    u.tmB[1] = u.tmB[0];
+    u.out2 = h;
+    set_out_maps(u, P.T, P.n, 2, 1);
+    ProfScope ps(s, K_UP_GLU, 2.0 * P.T * P.kr * P.n,
+                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n + P.T * P.n));
+    e = launch_gemm_rows(P.up, EPI_UPGLU, u, sms, s);
+  } else {
+    ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
+                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
+    e = launch_gemm_rows(P.up, EPI_BF16, u, sms, s);
+  }
+  return e;
+}
+
 // Forward of one block. With `glu` (k == 2: gate and up groups) the up-projection
 // computes both groups of a tile in one kernel and its epilogue also writes
 // h = silu(gate) * up. With `payload` non-NULL the down-projection runs as the explicit
@@ -578,41 +621,7 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
   // K3: y[i] = a[:, group i] @ B[i], batched over the k groups.
-  GemmParams u = base_params(P, err);
-  if (!make_map(&u.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, P.up.a_rows()))
-    return BOOST_ERR_CUDA;
-  if (!make_map(&u.tmB[0], B, P.n, P.r, P.k, P.n * 2, P.r * P.n * 2, 64, 64, 1))
-    return BOOST_ERR_CUDA;
-  u.seg[0].a = OperandView{2, 0, 1, 0};   // a as (r, k, T): K-major, batch = group
-  u.seg[0].b = OperandView{0, 1, 2, 1};   // B as (n, r, k): MN-major
-  u.seg[0].num_kb = static_cast<int32_t>(cdiv(P.r, kBK));
-  u.M = static_cast<int32_t>(P.T);
-  u.N = static_cast<int32_t>(P.n);
-  u.batch = static_cast<int32_t>(P.k);
-  u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.up.super_n()));
-  u.m_inner = 0;
-  u.out = y;
-  u.ldo = P.n;
-  u.out_bstride = P.T * P.n;
-  if (glu) {
-    // one tile list; segment 0 = the gate group into accumulator 0, segment 1 = the up
-    // group (same maps, batch index + 1) into accumulator 1
-    u.batch = 1;
-    u.num_seg = 2;
-    u.seg[1] = u.seg[0];
-    u.seg[1].batch_add = 1;
-    u.tmA[1] = u.tmA[0];
-    u.tmB[1] = u.tmB[0];
-    u.out2 = h;
-    set_out_maps(u, P.T, P.n, 2, 1);
-    ProfScope ps(s, K_UP_GLU, 2.0 * P.T * P.kr * P.n,
-                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n + P.T * P.n));
-    e = launch_gemm_rows(P.up, EPI_UPGLU, u, sms, s);
-  } else {
-    ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
-                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
-    e = launch_gemm_rows(P.up, EPI_BF16, u, sms, s);
-  }
+  e = launch_up(P, a, B, y, h, glu, err, sms, s);
   return cuda_status(e);
 }
 
@@ -625,6 +634,25 @@ boost_status boost_block_fwd(const boost_block_desc* desc, const void* x, const 
                              size_t ws_bytes, void* stream) {
   return block_fwd_impl(desc, x, gamma, A, B, y, nullptr, false, rstd, nullptr, false, ws,
                         ws_bytes, stream);
+}
+
+boost_status boost_block_up(const boost_block_desc* desc, const void* a, const void* B, void* y,
+                            void* h, void* ws, size_t ws_bytes, void* stream) {
+  boost_status st = validate_desc(desc);
+  if (st != BOOST_OK) return st;
+  const boost_block_desc& D = *desc;
+  const bool glu = h != nullptr;
+  if (glu && D.k != 2) return BOOST_ERR_INVALID_ARG;
+  st = D.T == 0 ? check_ptrs({B}, {a, y, h}) : check_ptrs({a, B, y}, {h});
+  if (st != BOOST_OK) return st;
+  const int sms = current_num_sms();
+  const Plan P = make_plan(D, sms);
+  st = check_ws(ws, ws_bytes, P.total);
+  if (st != BOOST_OK) return st;
+  if (D.T == 0) return BOOST_OK;
+  const cudaError_t e = launch_up(P, a, B, y, h, glu, ws_at<DeviceError>(ws, 0), sms,
+                                  static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
 }
 
 boost_status boost_block_fwd_btp(const boost_block_desc* desc, const void* x, const void* gamma,

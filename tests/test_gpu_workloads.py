@@ -284,3 +284,30 @@ def test_svd_40b_pair_full_size_sampled_rows():
     assert_close("dx qkv rows", dxq, gq["dx"])
     assert_close("dx gu rows", dxg, gg["dx"])
     assert_close("dx rows", dx, dxq + dxg)
+
+
+@pytest.mark.parametrize("T,d,r,ffn", [(512, 256, 128, 512), (600, 128, 64, 520)])
+def test_bottleneck_checkpoint_cut_matches_the_input_cut(T, d, r, ffn):
+    # keeping only the gate/up bottleneck activation and regenerating gate, up and h in
+    # backward gives the input cut's gradients bit for bit (same kernels, same values)
+    w = inputs.make_mlp(T, d, r, ffn, seed=8)
+    x, dout = w["x"].cuda(), w["dout"].cuda()
+    res = []
+    for cut in ("input", "bottleneck"):
+        mlp = MLP(T, d, r, ffn, S=2, weights=w, checkpoint=cut)
+        out = mlp.forward(x).clone()
+        gate_up, h = mlp.gu.y.clone(), mlp.h.clone()
+        if cut == "bottleneck":          # what the forward left behind is not reused
+            mlp.gu.y.fill_(float("nan"))
+            mlp.h.fill_(float("nan"))
+        mlp.backward(x, dout)
+        B.check(mlp.gu.ws)
+        B.check(mlp.dn.ws)
+        res.append((out, gate_up, h, mlp.gu.y.clone(), mlp.h.clone(),
+                    {k: v.clone() for k, v in mlp.grads().items()}))
+    (o1, gu1, h1, _, _, g1), (o2, gu2, h2, gu2b, h2b, g2) = res
+    assert torch.equal(o1, o2)
+    assert torch.equal(gu2b, gu1) and torch.equal(h2b, h1)    # regenerated == forward's
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+    assert MLP(T, d, r, ffn, checkpoint="bottleneck", weights=w).saved_bytes() == T * 2 * r * 2
