@@ -418,6 +418,56 @@ cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g, int
   return e;
 }
 
+// Launch a GEMM whose rows are too few to split (the weight gradients, M = r or d): with
+// 2 x 2 clusters, the last output columns run as a CTA-pair launch on the SMs no
+// cluster fits, on the side stream. The column split minimises the larger of the two
+// launches' wave counts, a pair's 256 x 256 tile costing `cost` cluster super-tile waves
+// (a lone pair has no multicast partner and shares L2 with the cluster launch; 1.25
+// measured alone). BOOST_COSCHED_COLS sets the cost in percent, 0 turns this off.
+cudaError_t launch_gemm_cols(const Shape& sh, int mode, const GemmParams& g, int sms,
+                             cudaStream_t s) {
+  static const int cost_pct = env_int("BOOST_COSCHED_COLS", 125);
+  const double kPairTileCost = cost_pct / 100.0;
+  if (cost_pct <= 0 || sh.mcm * sh.mcn < 4 || g.group_tiles > 0 || g.n_base != 0)
+    return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
+  const int64_t r_main = gemm_resident(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, sms);
+  const int64_t r_side = (sms - r_main * sh.cg * sh.mcm * sh.mcn) / 2;
+  const int64_t super_n = sh.super_n();
+  const int64_t n_super = cdiv(g.N, super_n);
+  if (r_main <= 0 || r_side <= 0 || n_super < 2)
+    return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
+  const int64_t units = static_cast<int64_t>(g.batch) * g.splits;
+  const int64_t m_super = cdiv(g.M, sh.super_m()), m_pair = cdiv(g.M, 256);
+  double best = static_cast<double>(cdiv(units * m_super * n_super, r_main));
+  int64_t best_nm = n_super;
+  for (int64_t nm = 1; nm < n_super; ++nm) {
+    const double t_main = static_cast<double>(cdiv(units * m_super * nm, r_main));
+    const int64_t side_tiles = units * m_pair * cdiv(g.N - nm * super_n, sh.bn);
+    const double t_side = static_cast<double>(cdiv(side_tiles, r_side)) * kPairTileCost;
+    const double t = std::max(t_main, t_side);
+    if (t < best * 0.999) {
+      best = t;
+      best_nm = nm;
+    }
+  }
+  if (best_nm == n_super) return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
+  CoStreams* cs = co_streams();
+  if (cs == nullptr) return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
+  GemmParams a = g, b = g;
+  a.n_tiles = static_cast<int32_t>(best_nm);
+  b.n_base = static_cast<int32_t>(best_nm * super_n);
+  b.n_tiles = static_cast<int32_t>(cdiv(g.N - b.n_base, sh.bn));
+  std::lock_guard<std::mutex> lk(cs->order);
+  cudaError_t e = cudaEventRecord(cs->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->side, cs->fork, 0);
+  if (e == cudaSuccess) e = launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, a, sms, s);
+  if (e == cudaSuccess) e = launch_gemm(sh.bn, mode, 2, 1, 1, b, sms, cs->side);
+  if (e == cudaSuccess) prof_note_kernels(1);
+  if (e == cudaSuccess) e = cudaEventRecord(cs->join, cs->side);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, cs->join, 0);
+  return e;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -792,7 +842,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.out_sstride = P.k * P.r * P.n;
       {
         ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-        e = launch_gemm(P.wB.bn, EPI_F32, P.wB.cg, P.wB.mcm, P.wB.mcn, w, sms, s);
+        e = launch_gemm_cols(P.wB, EPI_F32, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
@@ -801,7 +851,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
     } else {
       w.out = dB;
       ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-      e = launch_gemm(P.wB.bn, EPI_BF16, P.wB.cg, P.wB.mcm, P.wB.mcn, w, sms, s);
+      e = launch_gemm_cols(P.wB, EPI_BF16, w, sms, s);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
   }
@@ -826,7 +876,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.out_sstride = P.d * P.kr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.wA.bn, EPI_F32, P.wA.cg, P.wA.mcm, P.wA.mcn, w, sms, s);
+        e = launch_gemm_cols(P.wA, EPI_F32, w, sms, s);
       }
       if (e == cudaSuccess) {
         ProfScope ps(s, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
@@ -840,7 +890,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
       {
         ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm(P.wA.bn, EPI_DA, P.wA.cg, P.wA.mcm, P.wA.mcn, w, sms, s);
+        e = launch_gemm_cols(P.wA, EPI_DA, w, sms, s);
       }
       if (e == cudaSuccess && D.has_norm) {
         ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * P.n_cols_wA * P.d + 2.0 * P.d);

@@ -87,6 +87,8 @@ struct GemmParams {
   int32_t m_tiles, n_tiles;
   int32_t m_base;             // first output row of this launch (rows [m_base, m_base+m_extent))
   int32_t m_extent;           // rows of this launch (0: all of M from m_base)
+  int32_t n_base;             // first output column of this launch (ungrouped tiling;
+                              // a multiple of the launch's tile width)
   int32_t splits, kb_per_split;
   int32_t m_inner;            // tile order: 1 = m fastest within (batch, split)
   int32_t group_n;            // columns per group (grouped tiling)
@@ -200,14 +202,14 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int32_t ti
   c.split = bs / p.batch;
   c.batch = bs - c.split * p.batch;
   c.m0 = p.m_base + mb * TILE_M;
-  c.n_blk = nb;
+  c.n_blk = nb + p.n_base / BN;   // column-tile index over the whole output
   if (p.group_tiles > 0) {
     c.group = nb / p.group_tiles;
     c.n_local = (nb - c.group * p.group_tiles) * BN;
     c.n0 = c.group * p.group_n + c.n_local;
     c.n_end = min(c.n0 + BN, (c.group + 1) * p.group_n);
   } else {
-    c.n0 = nb * BN;
+    c.n0 = p.n_base + nb * BN;
     c.n_end = min(c.n0 + BN, p.N);
     c.group = 0;
     c.n_local = c.n0;

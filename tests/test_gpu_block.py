@@ -62,6 +62,8 @@ CASES = [
     # >= 8 row super-tiles of 2 x 2 clusters: the row GEMMs split their last rows
     # into a concurrent CTA-pair launch; T is not a multiple of either launch's tile
     ("co_scheduled_rows", 4352, 512, 512, 2, 1024, 4, "silu", True),
+    # dB's 16 column super-tiles split between the cluster launch and a pair launch
+    ("co_scheduled_cols", 1024, 256, 512, 2, 8192, 4, "silu", True),
 ]
 
 
@@ -125,6 +127,27 @@ def test_co_scheduled_gemms_count_two_kernels():
         assert kernels[name] == 2, name
     for name in ("gemm_wgrad_A", "gemm_wgrad_B", "rmsnorm_stats"):
         assert kernels[name] == ops[name][0], name
+
+
+@pytest.mark.skipif(os.environ.get("BOOST_COSCHED_COLS", "") == "0",
+                    reason="column co-scheduling turned off in the environment")
+def test_weight_gradient_columns_are_co_scheduled():
+    # dB = a^T dy has M = r = 512 rows (one super-tile row) and 16 column super-tiles:
+    # its last columns run as a CTA-pair launch beside the cluster launch
+    T, d, r, k, n, S = 1024, 256, 512, 2, 8192, 4
+    w = inputs.make_block(T, d, r, k, n, seed=9)
+    blk = Block(T, d, r, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    B.profile_enable(True)
+    try:
+        blk.forward(x)
+        blk.backward(x, dy)
+        torch.cuda.synchronize()
+        ops = B.profile_read()
+        kernels = B.profile_kernels()
+    finally:
+        B.profile_enable(False)
+    assert ops["gemm_wgrad_B"][0] == 1 and kernels["gemm_wgrad_B"] == 2
 
 
 def test_backward_with_and_without_saved_rstd_agree():
