@@ -69,3 +69,33 @@ def test_payload_size_is_exact():
     assert B.btp_payload_elems(desc) == 4 * oracle.exchange_elems(128, 3, 64)
     nonorm = B.make_desc(128, 256, 64, 3, 256, S=4, has_norm=False)
     assert B.btp_payload_elems(nonorm) == 4 * 128 * 3 * 64
+
+
+@pytest.mark.slow
+def test_exchange_at_the_7b_gate_up_block_size_sampled_rows():
+    """The benchmarked gate/up block (T=16384, d=4096, r=1024, k=2, n=11008, S=8):
+    every shard's partials and sums of squares and the block output on sampled rows
+    (rows are independent in the forward) against the oracle on those rows."""
+    c = inputs.CONFIGS["llama2_7b_mlp"]
+    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
+    w = inputs.make_block(T, d, r, 2, ffn, seed=23)
+    blk = Block(T, d, r, 2, ffn, S=S, weights=w)
+    x = w["x"].cuda()
+    y, zpart, ssq = B.block_fwd_btp(blk.desc, x, blk.gamma, blk.A, blk.B, blk.ws)
+    B.check(blk.ws)
+    rows = np.sort(np.random.default_rng(0).choice(T, 96, replace=False))
+    rows = np.concatenate([[0], rows, [T - 1]])
+    idx = torch.as_tensor(rows, device="cuda")
+    zs = zpart.index_select(1, idx).cpu()
+    qs = ssq.index_select(1, idx).cpu()
+    ys = y.index_select(1, idx).cpu()
+    del y, zpart, ssq, blk
+    torch.cuda.empty_cache()
+    X = inputs.as_f64(w["x"])[rows]
+    G, A, Bw = (inputs.as_f64(w[k]) for k in ("gamma", "A", "B"))
+    o_z, o_q = oracle.btp_shard_partials(X, G, A, S)
+    for s in range(S):
+        assert_close(f"zpart[{s}]", zs[s], o_z[s], 1e-4, 1e-5)
+    np.testing.assert_allclose(qs.double().numpy(), o_q, rtol=2e-5, atol=1e-6)
+    o_y, _ = oracle.block_fwd(X, G, A, Bw, S=S)
+    assert_close("y", ys, o_y)

@@ -311,3 +311,29 @@ def test_bottleneck_checkpoint_cut_matches_the_input_cut(T, d, r, ffn):
     for k in g1:
         assert torch.equal(g1[k], g2[k]), k
     assert MLP(T, d, r, ffn, checkpoint="bottleneck", weights=w).saved_bytes() == T * 2 * r * 2
+
+
+@pytest.mark.slow
+def test_bottleneck_checkpoint_cut_at_the_7b_mlp_size():
+    """Both checkpoint cuts of the benchmarked MLP give identical outputs and gradients."""
+    c = inputs.CONFIGS["llama2_7b_mlp"]
+    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
+    w = inputs.make_mlp(T, d, r, ffn, seed=12)
+    x, dout = w["x"].cuda(), w["dout"].cuda()
+    res = []
+    for cut in ("input", "bottleneck"):
+        mlp = MLP(T, d, r, ffn, S=S, weights=w, checkpoint=cut)
+        out = mlp.forward(x).clone()
+        if cut == "bottleneck":
+            mlp.gu.y.fill_(float("nan"))
+            mlp.h.fill_(float("nan"))
+        mlp.backward(x, dout)
+        B.check(mlp.gu.ws)
+        B.check(mlp.dn.ws)
+        res.append((out, {k: v.clone() for k, v in mlp.grads().items()}))
+        del mlp
+        torch.cuda.empty_cache()
+    (o1, g1), (o2, g2) = res
+    assert torch.equal(o1, o2)
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
