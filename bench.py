@@ -36,12 +36,39 @@ CPU_SAMPLE_T = 1024          # tokens of the CPU-baseline sample (full d, r, ffn
 REF_STEP_T = 16              # tokens per step of the reference arm
 
 
-def mlp_flops(T, d, r, ffn):
-    """Executed flops of one MLP step (recompute included) and model flops."""
-    blocks = [(d, 2 * r, ffn), (ffn, r, d)]          # (input width, k*r, n)
+def _flops(T, blocks):
+    """Executed flops of one fwd + bwd step over bottleneck blocks (input width, k*r, n),
+    the recompute of z included, and model flops (without it)."""
     exe = sum(8 * T * din * kr + 6 * T * kr * n for din, kr, n in blocks)
     model = sum(6 * T * din * kr + 6 * T * kr * n for din, kr, n in blocks)
     return exe, model
+
+
+def mlp_flops(T, d, r, ffn):
+    """Executed flops of one MLP step (recompute included) and model flops."""
+    return _flops(T, [(d, 2 * r, ffn), (ffn, r, d)])
+
+
+def workload_blocks(name):
+    """(input width, k*r, n) of every bottleneck block in a step of a named workload."""
+    from rank_bottleneck_online_gb300.inputs import CONFIGS
+
+    c = CONFIGS[name]
+    d, r = c["d"], c["r"]
+    kind = c["kind"]
+    if kind == "block":
+        return [(d, c["k"] * r, c["n"])]
+    if kind == "mlp":
+        return [(d, 2 * r, c["ffn"]), (c["ffn"], r, d)]
+    if kind == "layer":       # QKV, O (input: the attention stand-in V), gate/up, down
+        return [(d, 3 * r, d), (d, r, d), (d, 2 * r, c["ffn"]), (c["ffn"], r, d)]
+    if kind == "svd_pair":    # QKV and gate/up on one x
+        return [(d, 3 * r, d), (d, 2 * r, c["ffn"])]
+    raise KeyError(name)
+
+
+def workload_flops(name, T):
+    return _flops(T, workload_blocks(name))
 
 
 def dense_mlp_flops(T, d, ffn):
@@ -154,9 +181,9 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def _cfg():
+def _cfg(name=WORKLOAD):
     from rank_bottleneck_online_gb300.inputs import CONFIGS
-    return CONFIGS[WORKLOAD]
+    return CONFIGS[name]
 
 
 # ------------------------------------------------------------- clocks
@@ -337,30 +364,77 @@ def read_traffic(kernel, units):
     return None
 
 
+def _workspaces(wl):
+    """The distinct workspaces of a workload object and its blocks."""
+    seen, out = set(), []
+    stack = [wl]
+    while stack:
+        o = stack.pop()
+        ws = getattr(o, "ws", None)
+        if ws is not None and id(ws) not in seen:
+            seen.add(id(ws))
+            out.append(ws)
+        for name in ("gu", "dn", "qkv", "o", "mlp"):
+            sub = getattr(o, name, None)
+            if sub is not None:
+                stack.append(sub)
+    return out
+
+
+def _workload_step(name, wl, w, dev):
+    """forward + backward of one step of a named workload on device inputs."""
+    from rank_bottleneck_online_gb300.inputs import CONFIGS
+
+    kind = CONFIGS[name]["kind"]
+    x = w["x"].to(dev)
+    if kind == "block":
+        dy = w["dy"].to(dev)
+        return lambda: (wl.forward(x), wl.backward(x, dy))
+    if kind == "mlp":
+        dout = w["dout"].to(dev)
+        return lambda: (wl.forward(x), wl.backward(x, dout))
+    if kind == "layer":
+        dout, dq, dk = (w[k].to(dev) for k in ("dout", "dq", "dk"))
+        return lambda: (wl.forward(x), wl.backward(x, dout, dq, dk))
+    dq, dg = w["dy_qkv"].to(dev), w["dy_gu"].to(dev)
+    return lambda: (wl.forward(x), wl.backward(x, dq, dg))
+
+
 def ours_arm(args, rank, world, local_rank):
     import torch
 
     from rank_bottleneck_online_gb300 import binding as B
     from rank_bottleneck_online_gb300 import build as build_mod
     from rank_bottleneck_online_gb300 import inputs
-    from rank_bottleneck_online_gb300.block import MLP
+    from rank_bottleneck_online_gb300.block import MLP, build_workload
 
     build_mod.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    c = _cfg()
-    T, d, r, ffn, S = c["T"], c["d"], c["r"], c["ffn"], c["S"]
-    if args.tokens:
-        T = args.tokens
-    w = inputs.make_inputs(WORKLOAD, seed=0, T=T)
-    mlp = MLP(T, d, r, ffn, S=S, weights=w, device=dev)
-    x = w["x"].to(dev)
-    dout = w["dout"].to(dev)
+    name = args.workload
+    c = inputs.CONFIGS[name]
+    T = args.tokens or c["T"]
+    w = inputs.make_inputs(name, seed=0, T=T)
     stream = torch.cuda.current_stream()
+    mlp = None
+    if name == WORKLOAD:
+        d, r, ffn, S = c["d"], c["r"], c["ffn"], c["S"]
+        mlp = MLP(T, d, r, ffn, S=S, weights=w, device=dev)
+        x = w["x"].to(dev)
+        dout = w["dout"].to(dev)
+        wl = mlp
 
-    def step():
-        mlp.forward(x)
-        mlp.backward(x, dout)
+        def step():
+            mlp.forward(x)
+            mlp.backward(x, dout)
+    else:
+        wl = build_workload(name, w, device=dev, T=T)
+        step = _workload_step(name, wl, w, dev)
+    workspaces = _workspaces(wl)
+
+    def check():
+        for ws in workspaces:
+            B.check(ws)
 
     dist = None
     if world > 1:
@@ -372,7 +446,7 @@ def ours_arm(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         step()
-    B.check(mlp.gu.ws)
+    check()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
@@ -392,16 +466,20 @@ def ours_arm(args, rank, world, local_rank):
     prof = B.profile_read()
     prof_kernels = B.profile_kernels()
     B.profile_enable(False)
-    B.check(mlp.gu.ws)
+    check()
     ms_total = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    if mlp is None:             # the other workloads: the timed step and its roofline only
+        if rank != 0:
+            return 0
+        return _report(args, world, prof, prof_kernels, clocks, ms_total, float("nan"), 0, 0,
+                       T, c["d"], c["r"], c.get("ffn"), c["S"])
 
-    e2e_s = float("nan") if args.skip_aux else _e2e(args, mlp, w, x, dout, T, d, barrier,
-                                                    dist, dev)
-    btp = None if args.skip_aux or rank != 0 else _btp_exchange(mlp, x, T, d, r, ffn, S)
-    dense = (None if args.skip_aux or rank != 0
-             else _dense_context(T, d, ffn, ms_total / args.steps))
-    cuts = (None if args.skip_aux or rank != 0
-            else _checkpoint_cuts(mlp, w, x, dout, T, d, r, ffn, S, ms_total / args.steps))
+    aux = not args.skip_aux
+    e2e_s = _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev) if aux else float("nan")
+    btp = _btp_exchange(mlp, x, T, d, r, ffn, S) if aux and rank == 0 else None
+    dense = _dense_context(T, d, ffn, ms_total / args.steps) if aux and rank == 0 else None
+    cuts = (_checkpoint_cuts(mlp, w, x, dout, T, d, r, ffn, S, ms_total / args.steps)
+            if aux and rank == 0 else None)
     bi = 2 * T * d * 2          # x and dout, bf16
     bo = 2 * T * d * 2          # out and dx, bf16
     if rank != 0:
@@ -522,7 +600,8 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
             S, btp=None, dense=None, cuts=None):
     ms_step = ms_total / args.steps
     tokens_per_s = aggregate_rate(world, T * args.steps, ms_total / 1e3)
-    exe, model = mlp_flops(T, d, r, ffn)
+    default = args.workload == WORKLOAD
+    exe, model = workload_flops(args.workload, T)
     tflops = world * exe * args.steps / (ms_total / 1e3) / 1e12
     peaks = load_peaks()
     # dominant kernel: the largest share of the timed region (event time per kernel)
@@ -538,7 +617,8 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
         per_launch_units = kby / launches
-    traffic = read_traffic(name, per_launch_units)
+    # (the committed counters are for the default workload's shapes)
+    traffic = read_traffic(name, per_launch_units) if default else None
     step_bytes = sum(v[3] for v in prof.values()) / args.steps
     roof_ms = max(exe / (peaks["bf16_tflops"] * 1e12),
                   step_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
@@ -546,7 +626,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     gpu_launches = sum(prof_kernels.get(k, v[0]) for k, v in prof.items())
 
     cpu = None
-    if world == 1 and not args.skip_aux:
+    if world == 1 and not args.skip_aux and default:
         try:
             res = cpu_oracle_sample(CPU_SAMPLE_T, steps=1)
             cpu = {"value": CPU_SAMPLE_T / res["seconds"][0], "unit": "tokens/s",
@@ -568,7 +648,9 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": T, "d": d, "r": r, "ffn": ffn, "S": S,
+        "config": {"workload": args.workload, "tokens": T, "d": d, "r": r,
+                   **({"ffn": ffn} if ffn else {}), "S": S,
+                   **({k: v for k, v in _cfg(args.workload).items() if k in ("k", "n", "kind")}),
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (no flush)"},
         "tflops_per_s": tflops,
@@ -584,7 +666,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
                                    else peaks["source"])},
         "kernels": kernels,
         "gpu_launches": gpu_launches,
-        "e2e": None if args.skip_aux else {
+        "e2e": None if args.skip_aux or not default else {
             "value": aggregate_rate(world, T * args.steps, e2e_s), "unit": "tokens/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "clocks": clocks,
@@ -607,6 +689,11 @@ def main(argv=None):
                     help="run the workload on fewer tokens (profiling captures)")
     ap.add_argument("--skip-aux", action="store_true",
                     help="skip the end-to-end and CPU-baseline legs (profiling captures)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["llama2_1b_attn_block", "llama2_7b_mlp", "llama2_13b_layer",
+                             "svd_40b_pair", "tiny_block"],
+                    help="the timed step's workload; the metric's own is the default, the "
+                         "others report the step and its roofline only")
     ap.add_argument("--_oracle-sample", type=int, default=0, dest="oracle_sample")
     ap.add_argument("--_oracle-steps", type=int, default=1, dest="oracle_steps")
     args = ap.parse_args(argv)
@@ -618,6 +705,12 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
+        if args.workload != WORKLOAD:
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the oracle arm times the metric's own workload "
+                                  f"({WORKLOAD}) only"}), flush=True)
+            return 0
         return reference_arm(args, rank, world)
     if world > 1:
         import torch

@@ -380,10 +380,11 @@ CoStreams* co_streams() {
 // split the rows between that launch and a CTA-pair launch on a side stream.
 cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g, int sms,
                              cudaStream_t s) {
-  // rows of the side launch per 1000; 0 turns co-scheduling off. 160 measured best on the
-  // 4096-wide 7B MLP GEMMs (32 leftover SMs at roughly three quarters of the per-SM rate
-  // of the 8-CTA clusters).
-  static const int permille = env_int("BOOST_COSCHED", 160);
+  // rows of the side launch per 1000; 0 turns co-scheduling off. 130 measured best over
+  // the LLaMA-2 shapes (7B MLP: 130 = 160 > 100; 1B attention block: 130 > 100 > 160):
+  // the 32 leftover SMs run pair tiles at roughly three quarters of the per-SM rate of
+  // the 8-CTA clusters.
+  static const int permille = env_int("BOOST_COSCHED", 130);
   const int64_t M = g.M;
   const int64_t unit = sh.super_m();
   if (permille <= 0 || sh.mcm * sh.mcn < 4 || M < 8 * unit)

@@ -92,3 +92,17 @@ def test_dense_fullrank_context_is_the_textbook_mlp():
     dx = rs * (dxh - xh * (dxh * xh).mean(axis=1, keepdims=True))
     np.testing.assert_allclose(t["x"].grad.numpy(), dx, rtol=1e-10, atol=1e-12)
     assert bench.dense_mlp_flops(T, d, ffn) == 6.0 * T * 3 * d * ffn
+
+
+def test_workload_flop_model():
+    # the default workload's model is the MLP's; a single block is 8 T d kr + 6 T kr n
+    assert bench.workload_flops("llama2_7b_mlp", 16384) == bench.mlp_flops(16384, 4096, 1024,
+                                                                           11008)
+    exe, model = bench.workload_flops("llama2_1b_attn_block", 100)
+    assert exe == 8 * 100 * 2048 * 1536 + 6 * 100 * 1536 * 2048
+    assert model == 6 * 100 * 2048 * 1536 + 6 * 100 * 1536 * 2048
+    # the layer: QKV + O + the MLP's two blocks
+    lay, _ = bench.workload_flops("llama2_13b_layer", 1)
+    d, r, f = 5120, 1280, 13824
+    assert lay == sum(8 * di * kr + 6 * kr * n for di, kr, n in
+                      [(d, 3 * r, d), (d, r, d), (d, 2 * r, f), (f, r, d)])
