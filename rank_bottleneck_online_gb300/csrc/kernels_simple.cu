@@ -130,17 +130,63 @@ __global__ void __launch_bounds__(kThreads) btp_reduce_kernel(
   }
 }
 
+// The same statistics when every shard spans a multiple of 256 columns (32 lanes x 8
+// values): each lane's 16-byte pieces lane + 32 j of a row then fall, for every j, into
+// one shard for the whole warp, so a lane can issue eight loads before it reduces (a
+// row's loads in flight instead of two pieces per shard) and the shard boundaries stay
+// warp-uniform. Shards are reduced and combined in index order.
+__global__ void __launch_bounds__(kThreads) rmsnorm_stats_wide_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
+    float* __restrict__ ssq, float* __restrict__ rstd) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * d) + lane;
+  const int nj = static_cast<int>(d / 256);          // pieces per lane
+  const int jps = static_cast<int>(d / S / 256);     // pieces per lane per shard
+  float total = 0.0f, run = 0.0f;
+  int cur = 0;
+  for (int j0 = 0; j0 < nj; j0 += 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (j0 + k < nj) v[k] = __ldg(xr + 32 * (j0 + k));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (j0 + k >= nj) break;
+      const int sh = (j0 + k) / jps;               // warp-uniform
+      if (sh != cur) {
+        const float part = warp_sum(run);
+        if (lane == 0 && ssq != nullptr) ssq[static_cast<int64_t>(cur) * T + row] = part;
+        total += part;
+        run = 0.0f;
+        cur = sh;
+      }
+      float f[8];
+      unpack8(v[k], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) run = fmaf(f[e], f[e], run);
+    }
+  }
+  const float part = warp_sum(run);
+  if (lane == 0 && ssq != nullptr) ssq[static_cast<int64_t>(cur) * T + row] = part;
+  total += part;
+  if (lane == 0) rstd[row] = 1.0f / sqrtf(total / static_cast<float>(d) + eps);
+}
+
 // A'[j, m] = bf16(gamma_j * A[j, m]); the product of two bf16 values is exact in fp32.
+// Grid (column blocks, row blocks): rows j = blockIdx.y, blockIdx.y + gridDim.y, ...;
+// one 16-byte piece of the row per thread.
 __global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
     const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
     __nv_bfloat16* __restrict__ Ap, int64_t d, int64_t kr) {
-  const int64_t nvec = d * kr / 8;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
-       i += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int64_t j = (i * 8) / kr;
+  const int64_t v = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (v >= kr / 8) return;
+  for (int64_t j = blockIdx.y; j < d; j += gridDim.y) {
     const float g = __bfloat162float(gamma[j]);
+    const int64_t i = j * (kr / 8) + v;
     float f[8];
-    unpack8(reinterpret_cast<const uint4*>(A)[i], f);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(A) + i), f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] *= g;
     reinterpret_cast<uint4*>(Ap)[i] = pack8(f);
@@ -206,36 +252,38 @@ __global__ void __launch_bounds__(kThreads) splitk_sum_bf16_kernel(
   }
 }
 
-// One warp per row j of G = sum_s part[s] ([d, kr]): dA = bf16(gamma_j * G[j, :]) and
-// dgamma_j = bf16(sum_m A[j, m] * G[j, m]). Without gamma: dA = bf16(G).
+// One block per row j of G = sum_s part[s] ([d, kr], splits summed in order): dA =
+// bf16(gamma_j * G[j, :]) and dgamma_j = bf16(sum_m A[j, m] * G[j, m]), the row sum
+// reduced in a fixed order (per thread, then per warp, then over the warps). Without
+// gamma: dA = bf16(G). Each thread takes 8 columns at a time.
 __global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
     const float* __restrict__ part, int splits, int64_t d, int64_t kr,
     const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
     __nv_bfloat16* __restrict__ dA, __nv_bfloat16* __restrict__ dgamma) {
-  const int64_t j = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (j >= d) return;
+  __shared__ float wsum[kThreads / 32];
+  const int64_t j = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float g = gamma != nullptr ? __bfloat162float(gamma[j]) : 1.0f;
   const int64_t nv = kr / 8;
   const int64_t plane = d * kr;
   float acc = 0.0f;
-  for (int64_t i = lane; i < nv; i += 32) {
+  for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
     const int64_t off = j * kr + i * 8;
     float G[8];
-    const float4 a0 = *reinterpret_cast<const float4*>(part + off);
-    const float4 a1 = *reinterpret_cast<const float4*>(part + off + 4);
+    const float4 a0 = __ldg(reinterpret_cast<const float4*>(part + off));
+    const float4 a1 = __ldg(reinterpret_cast<const float4*>(part + off + 4));
     G[0] = a0.x; G[1] = a0.y; G[2] = a0.z; G[3] = a0.w;
     G[4] = a1.x; G[5] = a1.y; G[6] = a1.z; G[7] = a1.w;
-    for (int s = 1; s < splits; ++s) {
-      const float4 b0 = *reinterpret_cast<const float4*>(part + s * plane + off);
-      const float4 b1 = *reinterpret_cast<const float4*>(part + s * plane + off + 4);
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 b0 = __ldg(reinterpret_cast<const float4*>(part + sp * plane + off));
+      const float4 b1 = __ldg(reinterpret_cast<const float4*>(part + sp * plane + off + 4));
       G[0] += b0.x; G[1] += b0.y; G[2] += b0.z; G[3] += b0.w;
       G[4] += b1.x; G[5] += b1.y; G[6] += b1.z; G[7] += b1.w;
     }
     float o[8];
     if (gamma != nullptr) {
       float a[8];
-      unpack8(*reinterpret_cast<const uint4*>(A + off), a);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(A + off)), a);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         acc = fmaf(a[e], G[e], acc);
@@ -249,7 +297,13 @@ __global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
   }
   if (dgamma != nullptr) {
     acc = warp_sum(acc);
-    if (lane == 0) dgamma[j] = __float2bfloat16_rn(acc);
+    if (lane == 0) wsum[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.0f;
+      for (int w = 0; w < kThreads / 32; ++w) t += wsum[w];
+      dgamma[j] = __float2bfloat16_rn(t);
+    }
   }
 }
 
@@ -302,8 +356,12 @@ cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, flo
   if (T == 0) return cudaSuccess;
   const int rows_per_block = kThreads / 32;
   const int64_t grid = (T + rows_per_block - 1) / rows_per_block;
-  rmsnorm_stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
+  if ((d / S) % 256 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0)
+    rmsnorm_stats_wide_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
+  else
+    rmsnorm_stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
   return cudaGetLastError();
 }
 
@@ -319,7 +377,9 @@ cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64
 cudaError_t launch_fold_gamma(const void* gamma, const void* A, void* Ap, int64_t d, int64_t kr,
                               cudaStream_t stream) {
   if (d * kr == 0) return cudaSuccess;
-  fold_gamma_kernel<<<grid_for(d * kr / 8, kThreads), kThreads, 0, stream>>>(
+  const dim3 grid(static_cast<unsigned>((kr / 8 + kThreads - 1) / kThreads),
+                  static_cast<unsigned>(d < 65535 ? d : 65535));
+  fold_gamma_kernel<<<grid, kThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(A),
       static_cast<__nv_bfloat16*>(Ap), d, kr);
   return cudaGetLastError();
@@ -364,9 +424,7 @@ cudaError_t launch_splitk_finalize_dA(const float* part, int splits, int64_t d, 
                                       const void* gamma, const void* A, void* dA, void* dgamma,
                                       cudaStream_t stream) {
   if (d == 0) return cudaSuccess;
-  const int rows_per_block = kThreads / 32;
-  const int64_t grid = (d + rows_per_block - 1) / rows_per_block;
-  splitk_finalize_dA_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+  splitk_finalize_dA_kernel<<<static_cast<unsigned>(d), kThreads, 0, stream>>>(
       part, splits, d, kr, static_cast<const __nv_bfloat16*>(gamma),
       static_cast<const __nv_bfloat16*>(A), static_cast<__nv_bfloat16*>(dA),
       static_cast<__nv_bfloat16*>(dgamma));
