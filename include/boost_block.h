@@ -19,16 +19,31 @@
  *   `const void*` / `void*`) unless stated; fp32 tensors are `float*`.
  *   Device pointers must be device memory of the current device; host
  *   pointers are marked "host".
- * - The caller owns every buffer. The library allocates nothing, keeps no
- *   state between calls, and writes only to the outputs and the workspace.
+ * - The caller owns every buffer. The library allocates no device memory,
+ *   keeps no per-call state between calls, and writes only to the outputs and
+ *   the workspace. It holds a few per-device resources for the life of the
+ *   process, created on first use: a second stream and two events that let one
+ *   GEMM run as two concurrent launches over disjoint rows or columns
+ *   ("co-scheduling": a launch of 8-CTA clusters plus a CTA-pair launch on the
+ *   SMs no cluster fits), and cached cluster-occupancy counts
+ *   (boost_rmsnorm_rstd_noalloc adds its fixed array, below).
  * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
- *   stream). Every argument is validated on the host before anything is
- *   enqueued; a call that returns an error has enqueued nothing.
+ *   stream): a co-scheduled GEMM forks from `stream` to the side stream and joins
+ *   back with events, so everything a call enqueues is ordered after earlier
+ *   work on `stream` and before later work on it. Calls may be captured into
+ *   CUDA graphs (the fork and join become part of the capture). Every argument
+ *   is validated on the host before anything is enqueued: a call that returns
+ *   BOOST_ERR_INVALID_ARG, _UNSUPPORTED_SHAPE, _ALIGNMENT or _WORKSPACE has
+ *   enqueued nothing; BOOST_ERR_CUDA (a launch refused by the runtime) may
+ *   leave the first steps of the call enqueued.
  * - Device pointers must be 16-byte aligned. d, k*r, n (and r) must be
  *   multiples of 8 so that every row starts on a 16-byte boundary.
  * - Errors found on the device (a bounded wait that ran out) are recorded in
  *   the workspace's error word and reported by boost_block_check().
- * - Thread safety: calls on different workspaces may run concurrently.
+ * - Thread safety: calls on different workspaces may run concurrently; the
+ *   fork/launch/join sequences on the shared side stream are serialised
+ *   internally. Two threads capturing graphs on different streams at the same
+ *   time would both capture the side stream: do not overlap such captures.
  */
 #ifndef BOOST_BLOCK_H
 #define BOOST_BLOCK_H

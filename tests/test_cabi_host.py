@@ -172,3 +172,34 @@ def test_workspace_size_grows_with_shape(L):
     assert 0 < small < big
     # a, dzs [T, kr] bf16 and A' [d, kr] bf16 at least
     assert big >= 2 * 16384 * 1536 * 2 + 2048 * 1536 * 2
+
+
+def test_empty_token_batch_is_a_no_op_for_every_forward_entry(L):
+    # T = 0: the [T, ...] tensors are empty and may be NULL; nothing is enqueued
+    f = _fake
+    desc = B.make_desc(0, 256, 64, 2, 256, S=4)
+    ws_bytes = B.workspace_bytes(desc)
+    assert ws_bytes > 0
+    assert L.boost_block_fwd(ctypes.byref(desc), None, f(0x2000), f(0x3000), f(0x4000), None,
+                             None, f(0x100000), ws_bytes, None) == 0
+    assert L.boost_block_fwd_swiglu(ctypes.byref(desc), None, f(0x2000), f(0x3000), f(0x4000),
+                                    None, None, None, f(0x100000), ws_bytes, None) == 0
+    assert L.boost_block_fwd_btp(ctypes.byref(desc), None, f(0x2000), f(0x3000), f(0x4000),
+                                 None, None, None, f(0x100000), ws_bytes, None) == 0
+    assert L.boost_block_up(ctypes.byref(desc), None, f(0x4000), None, None, f(0x100000),
+                            ws_bytes, None) == 0
+
+
+def test_bottleneck_up_projection_argument_checks(L):
+    f = _fake
+    desc = B.make_desc(128, 256, 64, 3, 256, S=4)
+    ws_bytes = B.workspace_bytes(desc)
+    # h (the fused SwiGLU output) needs the gate and up groups: k == 2
+    assert L.boost_block_up(ctypes.byref(desc), f(0x1000), f(0x2000), f(0x3000), f(0x4000),
+                            f(0x100000), ws_bytes, None) == 1
+    assert L.boost_block_up(ctypes.byref(desc), None, f(0x2000), f(0x3000), None, f(0x100000),
+                            ws_bytes, None) == 1          # a missing
+    assert L.boost_block_up(ctypes.byref(desc), f(0x1008), f(0x2000), f(0x3000), None,
+                            f(0x100000), ws_bytes, None) == 3   # a misaligned
+    assert L.boost_block_up(ctypes.byref(desc), f(0x1000), f(0x2000), f(0x3000), None,
+                            f(0x100000), 64, None) == 4          # workspace too small
