@@ -224,3 +224,38 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     # the context still runs real work afterwards
     _, blk, _, _ = _run_block("after_timeout", 128, 128, 64, 1, 64, 2, "silu", True)
     assert torch.isfinite(blk.y.float()).all()
+
+
+def test_forward_backward_replay_from_a_cuda_graph():
+    # the calls are stream-ordered, so one step captures into a CUDA graph (the
+    # co-scheduled GEMMs' fork to and join from the side stream included) and replays
+    # to the eager results bit for bit
+    T, d, r, k, n, S = 4352, 512, 512, 2, 1024, 4
+    w = inputs.make_block(T, d, r, k, n, seed=13)
+    blk = Block(T, d, r, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+
+    def step():
+        blk.forward(x)
+        blk.backward(x, dy)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma)]
+    for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma):
+        t.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # warm-up on the capture stream
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma):
+        t.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    B.check(blk.ws)
+    for a, b in zip(eager, (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma)):
+        assert torch.equal(a, b)
