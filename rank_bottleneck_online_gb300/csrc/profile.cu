@@ -3,7 +3,10 @@
 // When enabled, every kernel launch is bracketed by two CUDA events recorded on
 // the launch's stream, and the launch's algorithmic work (flops and bytes, from the
 // shapes) is accumulated per kernel. Reading the counters synchronises the pending
-// events. Disabled (the default), a launch pays one relaxed atomic load.
+// events. Disabled (the default), a launch pays one relaxed atomic load. While the
+// stream is being captured into a CUDA graph the events become event-record nodes of
+// the graph (recorded when the graph runs), so a graph captured with timing enabled
+// and launched once yields one sample per captured launch.
 #include "profile.h"
 
 #include <atomic>
@@ -74,6 +77,14 @@ void drain_locked() {
   g_pending.clear();
 }
 
+void record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 }  // namespace
 
 ProfScope::ProfScope(cudaStream_t s, int id, double flops, double bytes)
@@ -83,7 +94,7 @@ ProfScope::ProfScope(cudaStream_t s, int id, double flops, double bytes)
   e0_ = take_event();
   e1_ = take_event();
   if (e0_ && e1_) {
-    cudaEventRecord(e0_, stream_);
+    record(e0_, stream_);
     active_ = true;
     outer_ = t_open;
     t_open = this;
@@ -94,7 +105,7 @@ ProfScope::~ProfScope() {
   if (!active_) return;
   t_open = outer_;
   std::lock_guard<std::mutex> lk(g_mu);
-  cudaEventRecord(e1_, stream_);
+  record(e1_, stream_);
   g_pending.push_back(Pending{id_, e0_, e1_, flops_, bytes_, kernels_});
 }
 
