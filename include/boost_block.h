@@ -332,6 +332,10 @@ boost_status boost_debug_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_
  *   spanning both.
  *   boost_profile_read_kernels(id, &kernels) returns the number of kernels those
  *   operations launched (>= the launch count). kernels must not be NULL.
+ * While the stream is being captured into a CUDA graph, the events become the
+ * graph's event-record nodes: launch such a graph once, then read the counters
+ * (reading returns the events to a pool that later operations reuse, so a graph
+ * launched again after that no longer times its own operations).
  * Process-wide; intended for one measuring thread.
  */
 boost_status boost_profile_enable(int on);
