@@ -927,10 +927,6 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
     if (glu) {
       w.out = dgate;
       w.out2 = dup;
-      w.gate = static_cast<const __nv_bfloat16*>(gate);
-      w.up = static_cast<const __nv_bfloat16*>(up);
-    }
-    if (glu) {
       set_out_maps(w, P.T, P.d, 1, 1);
       // the epilogue streams gate and up through TMA (required by this mode)
       if (!make_map(&w.tmE[0], gate, P.d, P.T, 1, P.d * 2, P.T * P.d * 2, 32, 32, 1, true) ||
@@ -943,7 +939,6 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.qpart = qpart;
       w.nq = P.n_cols_dual;
       w.d_norm = static_cast<int32_t>(P.d);
-      w.xin = static_cast<const __nv_bfloat16*>(x);
       // the RMSNorm term's x streams through TMA
       if (!make_map(&w.tmE[0], x, P.d, P.T, 1, P.d * 2, P.T * P.d * 2, 32, 32, 1, true))
         return BOOST_ERR_CUDA;

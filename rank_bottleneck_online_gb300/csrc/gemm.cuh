@@ -77,7 +77,8 @@ struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
   CUtensorMap tmO[2];         // bf16 outputs out / out2 as (cols, rows, batch), 32 x 32 boxes
-  CUtensorMap tmE[2];         // bf16 epilogue inputs (EPI_GLU: gate, up; EPI_DX: x), 32 x 32
+  CUtensorMap tmE[2];         // bf16 epilogue inputs shaped like the output, 32 x 32 boxes
+                              // (EPI_GLU: gate, up; EPI_DX: x)
   int32_t tma_out;            // bit i: tmO[i] is valid (else plain stores)
   int32_t tma_in;             // 1: the epilogue inputs stream through tmE (EPI_GLU: required)
   Segment seg[2];
@@ -105,11 +106,8 @@ struct GemmParams {
   const float* rstd;          // [M] row scale or nullptr (s == 1)
   float* qpart;               // EPI_DUAL out / EPI_DX in: [n_tiles or nq][M]
   float* dgpart;              // EPI_DA out: [n_tiles][M]
-  const __nv_bfloat16* xin;   // EPI_DX: x [M, N]
   const __nv_bfloat16* gamma; // EPI_DA: gamma [M]
   const __nv_bfloat16* wA;    // EPI_DA: A [M, N]
-  const __nv_bfloat16* gate;  // EPI_GLU: gate [M, N]
-  const __nv_bfloat16* up;    // EPI_GLU: up [M, N]
   DeviceError* err;
   uint64_t wait_limit_ns;
 };
