@@ -1,0 +1,116 @@
+"""Out-of-bounds write checks (compute-sanitizer is not available): every output
+buffer and the workspace sit between guard regions filled with a sentinel byte, and
+after forward and backward (plain, fused SwiGLU, emulated exchange) the guards must be
+untouched. Shapes with ragged row and column tiles, groups that are not a multiple of
+the tile width, and co-scheduled row and column splits.
+"""
+
+import math
+
+import pytest
+import torch
+
+from rank_bottleneck_online_gb300 import binding as B
+from rank_bottleneck_online_gb300 import build as build_mod
+from rank_bottleneck_online_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096          # bytes on each side; keeps the interior 256-byte aligned
+SENTINEL = 0xA5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_mod.build()
+    B.lib()
+
+
+class Guarded:
+    def __init__(self, shape, dtype):
+        self.nbytes = math.prod(shape) * torch.tensor([], dtype=dtype).element_size()
+        body = (self.nbytes + 255) // 256 * 256
+        self.raw = torch.full((2 * GUARD + body,), SENTINEL, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[GUARD:GUARD + self.nbytes].view(dtype).view(shape)
+
+    def intact(self):
+        return bool((self.raw[:GUARD] == SENTINEL).all()) and \
+            bool((self.raw[GUARD + self.nbytes:] == SENTINEL).all())
+
+
+def guarded_ws(desc):
+    g = Guarded((B.workspace_bytes(desc),), torch.uint8)
+    ws = B.Workspace.__new__(B.Workspace)
+    ws.nbytes, ws.buf = g.nbytes, g.t
+    B._check(B.lib().boost_block_ws_init(ws.ptr, ws.nbytes, B._stream()), "ws_init")
+    return g, ws
+
+
+CASES = [
+    # name, T, d, r, k, n, S, has_norm
+    ("ragged_rows_and_columns", 200, 192, 64, 2, 200, 4, True),
+    ("rank_not_tile_multiple", 72, 128, 40, 3, 72, 2, True),
+    ("no_norm_tail", 130, 128, 64, 1, 64, 2, False),
+    ("co_scheduled_rows", 4352, 512, 512, 2, 1024, 4, True),
+    ("co_scheduled_columns", 1024, 256, 512, 2, 8192, 4, True),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_no_write_outside_any_output(case):
+    _, T, d, r, k, n, S, norm = case
+    w = inputs.make_block(T, d, r, k, n, has_norm=norm, seed=31)
+    desc = B.make_desc(T, d, r, k, n, S=S, has_norm=norm)
+    bf, f32 = torch.bfloat16, torch.float32
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    A, Bw = w["A"].cuda(), w["B"].cuda()
+    gamma = w["gamma"].cuda() if norm else None
+    gws, ws = guarded_ws(desc)
+    outs = {"y": Guarded((k, T, n), bf), "dx": Guarded((T, d), bf),
+            "dA": Guarded((d, k * r), bf), "dB": Guarded((k, r, n), bf)}
+    if norm:
+        outs["rstd"] = Guarded((T,), f32)
+        outs["dgamma"] = Guarded((d,), bf)
+    rstd = outs["rstd"].t if norm else None
+    B.block_fwd(desc, x, gamma, A, Bw, ws, y=outs["y"].t, rstd=rstd)
+    B.block_bwd(desc, x, gamma, A, Bw, dy, ws, rstd=rstd, dx=outs["dx"].t,
+                dgamma=outs["dgamma"].t if norm else None, dA=outs["dA"].t, dB=outs["dB"].t)
+    if d % S == 0 and (d // S) % 64 == 0:
+        pay = Guarded((B.btp_payload_elems(desc),), f32)
+        B.block_fwd_btp(desc, x, gamma, A, Bw, ws, y=outs["y"].t, payload=pay.t)
+        outs["payload"] = pay
+    if k == 2:
+        h = Guarded((T, n), bf)
+        B.block_fwd_swiglu(desc, x, gamma, A, Bw, ws, y=outs["y"].t, h=h.t, rstd=rstd)
+        a = B.ws_view(ws, B.ws_layout(desc)["a"], (T, k * r), bf).clone()
+        B.block_up(desc, a, Bw, ws, y=outs["y"].t, h=h.t)
+        outs["h"] = h
+    torch.cuda.synchronize()
+    B.check(ws)
+    assert gws.intact(), "workspace guard overwritten"
+    for key, g in outs.items():
+        assert g.intact(), f"{key} guard overwritten"
+
+
+def test_no_write_outside_the_fused_swiglu_backward_outputs():
+    T, d, r, ffn = 4352, 256, 128, 520          # ragged last column tile, co-scheduled rows
+    w = inputs.make_mlp(T, d, r, ffn, seed=32)
+    desc = B.make_desc(T, ffn, r, 1, d, S=1, has_norm=False)
+    bf = torch.bfloat16
+    gws, ws = guarded_ws(desc)
+    h = torch.randn(T, ffn, device="cuda").to(bf)
+    gate = torch.randn(T, ffn, device="cuda").to(bf)
+    up = torch.randn(T, ffn, device="cuda").to(bf)
+    dy = w["dout"].cuda().view(1, T, d)
+    outs = {"dgate": Guarded((T, ffn), bf), "dup": Guarded((T, ffn), bf),
+            "dA": Guarded((ffn, r), bf), "dB": Guarded((1, r, d), bf)}
+    B.block_bwd_swiglu(desc, h, w["A2"].cuda(), w["B2"].cuda(), dy, gate, up, ws,
+                       dgate=outs["dgate"].t, dup=outs["dup"].t, dA=outs["dA"].t,
+                       dB=outs["dB"].t)
+    torch.cuda.synchronize()
+    B.check(ws)
+    assert gws.intact()
+    for key, g in outs.items():
+        assert g.intact(), f"{key} guard overwritten"
