@@ -307,6 +307,24 @@ boost_status boost_swiglu_bwd(int64_t T, int64_t n, const void* gate, const void
 boost_status boost_add(int64_t count, const void* a, const void* b, void* out, void* stream);
 
 /*
+ * Debug write counting, the tile-coverage check that stands in for a memory
+ * checker (the pages define nothing of the kind). boost_debug_count_writes(counts,
+ * capacity) starts recording: every tensor-core GEMM enqueued afterwards (by any
+ * entry point, on any stream) is given its own plane of `counts`, shaped like its
+ * output, and its epilogues atomically add 1 for each output element they write;
+ * boost_debug_count_writes(NULL, 0) stops. counts: device int32 [capacity], zeroed by
+ * the caller, 16-byte aligned. boost_debug_count_log(log, max_ops) returns the
+ * number of GEMM operations recorded (or -1 if `capacity` ran out, after which
+ * operations were left unrecorded) and copies up to max_ops entries of 8 int64 to
+ * host `log`: plane offset in counts, M, N, leading dimension, planes per split,
+ * splits, plane stride, split stride. Element (s, p, m, c) of an operation sits at
+ * offset + s*split_stride + p*plane_stride + m*ld + c; a correct tiling leaves 1 at
+ * every m < M, c < N and 0 in the padding c >= N. Process-wide; for tests.
+ */
+boost_status boost_debug_count_writes(int32_t* counts, int64_t capacity);
+int64_t boost_debug_count_log(int64_t* log, int64_t max_ops);
+
+/*
  * Self-test of the bounded wait every kernel uses (failure detection without a
  * GPU fault): launches one tiny kernel that waits on an mbarrier nothing
  * arrives on, with a wait limit of `limit_us` microseconds (1..10^6). The

@@ -33,7 +33,7 @@ EXPORTS = (
     "boost_block_ws_layout", "boost_profile_enable", "boost_profile_kernel_count",
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
     "boost_profile_read_kernels", "boost_block_fwd_swiglu", "boost_block_fwd_btp",
-    "boost_block_up",
+    "boost_block_up", "boost_debug_count_writes", "boost_debug_count_log",
 )
 
 
@@ -74,6 +74,9 @@ def lib():
     L.boost_block_fwd_swiglu.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_fwd_btp.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_block_up.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
+    L.boost_debug_count_writes.argtypes = [vp, i64]
+    L.boost_debug_count_log.argtypes = [ctypes.POINTER(i64), i64]
+    L.boost_debug_count_log.restype = i64
     L.boost_block_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_rmsnorm_stats.argtypes = [dp, vp, vp, vp, vp]
     L.boost_block_layout.argtypes = [dp, ctypes.POINTER(i64), ctypes.POINTER(i64),
@@ -96,7 +99,8 @@ def lib():
                                      ctypes.POINTER(i64), dbl, dbl, dbl]
     L.boost_profile_read_kernels.argtypes = [ctypes.c_int, ctypes.POINTER(i64)]
     for name in EXPORTS:
-        if name != "boost_block_workspace_bytes" and name != "boost_status_string":
+        if name not in ("boost_block_workspace_bytes", "boost_status_string",
+                        "boost_debug_count_log"):
             getattr(L, name).restype = ctypes.c_int
     _LIB = L
     return L
@@ -439,6 +443,29 @@ def profile_read():
         if n.value:
             out[name.value.decode()] = (n.value, ms.value, fl.value, by.value)
     return out
+
+
+def debug_count_writes(counts=None):
+    """Start (with a zeroed int32 CUDA tensor) or stop (None) write counting."""
+    if counts is None:
+        _check(lib().boost_debug_count_writes(None, 0), "boost_debug_count_writes")
+        return
+    if counts.dtype != torch.int32 or not counts.is_cuda or not counts.is_contiguous():
+        raise TypeError("counts must be a contiguous int32 CUDA tensor")
+    _check(lib().boost_debug_count_writes(_ptr(counts), counts.numel()),
+           "boost_debug_count_writes")
+
+
+def debug_count_log():
+    """[(offset, M, N, ld, planes, splits, plane_stride, split_stride)] of the recorded
+    GEMM operations; raises if the count buffer ran out."""
+    L = lib()
+    n = L.boost_debug_count_log(None, 0)
+    if n < 0:
+        raise RuntimeError("write-count buffer too small")
+    buf = (ctypes.c_int64 * (8 * max(n, 1)))()
+    L.boost_debug_count_log(buf, n)
+    return [tuple(buf[8 * i:8 * i + 8]) for i in range(n)]
 
 
 def debug_wait_timeout(ws: Workspace, limit_us: int, stream=None):

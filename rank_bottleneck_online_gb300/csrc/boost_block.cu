@@ -16,6 +16,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "profile.h"
@@ -351,6 +352,44 @@ bool down_segment(GemmParams& g, const Plan& P, const void* x, const void* Ap, c
   return true;
 }
 
+// ------------------------------------------------- write counting (debug)
+// While a caller has handed in a count buffer (boost_debug_count_writes), every GEMM
+// operation gets its own count plane, shaped like its output (split and batch planes
+// included), and its epilogues add 1 per element written; a log records each plane's
+// geometry so the caller can check that every output element is written exactly once.
+struct WriteCounter {
+  std::mutex mu;
+  int32_t* base = nullptr;
+  int64_t capacity = 0, cursor = 0;
+  bool overflow = false;
+  std::vector<int64_t> log;   // kLogFields values per operation
+};
+constexpr int kLogFields = 8;
+
+WriteCounter& write_counter() {
+  static WriteCounter w;
+  return w;
+}
+
+void attach_counts(GemmParams& g, int mode) {
+  WriteCounter& w = write_counter();
+  std::lock_guard<std::mutex> lk(w.mu);
+  if (w.base == nullptr) return;
+  const int64_t splits = std::max<int64_t>(g.splits, 1);
+  // the fused up-projection writes two batch planes (gate, up) from one tile list
+  const int64_t planes = mode == EPI_UPGLU ? 2 : std::max<int64_t>(g.batch, 1);
+  const int64_t extent = (splits - 1) * g.out_sstride + (planes - 1) * g.out_bstride +
+                         static_cast<int64_t>(g.M - 1) * g.ldo + g.N;
+  if (w.cursor + extent > w.capacity) {
+    w.overflow = true;
+    return;
+  }
+  g.visits = w.base + w.cursor;
+  w.log.insert(w.log.end(), {w.cursor, static_cast<int64_t>(g.M), static_cast<int64_t>(g.N),
+                             g.ldo, planes, splits, g.out_bstride, g.out_sstride});
+  w.cursor += extent;
+}
+
 // ------------------------------------------------------ co-scheduling
 // Launch shapes with clusters of eight CTAs leave SMs that no such cluster fits (152 SMs
 // hold 15 clusters of 8). For GEMMs over the token rows, the last rows of the output
@@ -387,8 +426,10 @@ CoStreams* co_streams() {
 
 // Launch one GEMM over its M rows; with co-scheduling enabled and a 2 x 2 cluster shape,
 // split the rows between that launch and a CTA-pair launch on a side stream.
-cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g, int sms,
+cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g_in, int sms,
                              cudaStream_t s) {
+  GemmParams g = g_in;
+  attach_counts(g, mode);
   // rows of the side launch per 1000; 0 turns co-scheduling off. 130 measured best over
   // the LLaMA-2 shapes (7B MLP: 130 = 160 > 100; 1B attention block: 130 > 100 > 160):
   // the 32 leftover SMs run pair tiles at roughly three quarters of the per-SM rate of
@@ -434,8 +475,10 @@ cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g, int
 // launches' wave counts, a pair's 256 x 256 tile costing `cost` cluster super-tile waves
 // (a lone pair has no multicast partner and shares L2 with the cluster launch; 1.25
 // measured alone). BOOST_COSCHED_COLS sets the cost in percent, 0 turns this off.
-cudaError_t launch_gemm_cols(const Shape& sh, int mode, const GemmParams& g, int sms,
+cudaError_t launch_gemm_cols(const Shape& sh, int mode, const GemmParams& g_in, int sms,
                              cudaStream_t s) {
+  GemmParams g = g_in;
+  attach_counts(g, mode);
   static const int cost_pct = env_int("BOOST_COSCHED_COLS", 125);
   const double kPairTileCost = cost_pct / 100.0;
   if (cost_pct <= 0 || sh.mcm * sh.mcn < 4 || g.group_tiles > 0 || g.n_base != 0)
@@ -983,6 +1026,30 @@ boost_status boost_block_ws_layout(const boost_block_desc* desc, size_t* off_a, 
   if (off_Ap) *off_Ap = P.off_Ap;
   if (off_rstd) *off_rstd = P.off_rstd;
   return BOOST_OK;
+}
+
+boost_status boost_debug_count_writes(int32_t* counts, int64_t capacity) {
+  if (counts != nullptr && (capacity <= 0 || !aligned16(counts))) return BOOST_ERR_INVALID_ARG;
+  WriteCounter& w = write_counter();
+  std::lock_guard<std::mutex> lk(w.mu);
+  w.base = counts;
+  w.capacity = counts != nullptr ? capacity : 0;
+  if (counts != nullptr) {
+    w.cursor = 0;
+    w.overflow = false;
+    w.log.clear();
+  }
+  return BOOST_OK;
+}
+
+int64_t boost_debug_count_log(int64_t* log, int64_t max_ops) {
+  WriteCounter& w = write_counter();
+  std::lock_guard<std::mutex> lk(w.mu);
+  if (w.overflow) return -1;
+  const int64_t ops = static_cast<int64_t>(w.log.size()) / kLogFields;
+  if (log != nullptr)
+    for (int64_t i = 0; i < std::min(ops, max_ops) * kLogFields; ++i) log[i] = w.log[i];
+  return ops;
 }
 
 boost_status boost_block_check(void* ws, void* stream) {

@@ -110,6 +110,7 @@ struct GemmParams {
   const __nv_bfloat16* wA;    // EPI_DA: A [M, N]
   DeviceError* err;
   uint64_t wait_limit_ns;
+  int32_t* visits;            // debug: per-element write counts, indexed like out (or NULL)
 };
 
 template <int BN, int MODE, int CG, int MCM = 1, int MCN = 1>
@@ -490,6 +491,16 @@ struct NoLoader {
   __device__ __forceinline__ void drain() {}
 };
 
+// Debug write counting: this lane's row of a 32 x 32 chunk whose element (0, 0) is at
+// index `base` of the output adds 1 to each element it writes.
+__device__ __forceinline__ void count_writes(const GemmParams& p, int64_t base, int lane,
+                                             int rows_valid, int cols_valid) {
+  if (lane < rows_valid) {
+    int32_t* v = p.visits + base + static_cast<int64_t>(lane) * p.ldo;
+    for (int c = 0; c < 32 && c < cols_valid; ++c) atomicAdd(v + c, 1);
+  }
+}
+
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
@@ -536,9 +547,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     if constexpr (MODE == EPI_DUAL) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
     tmem_ld_wait();
     if constexpr (MODE == EPI_F32) {
-      float* o = static_cast<float*>(p.out) + tc.split * p.out_sstride + tc.batch * p.out_bstride +
-                 static_cast<int64_t>(row0) * p.ldo + col0;
-      stage_store_f32(stg, lane, v, o, p.ldo, rows_valid, cols_valid);
+      const int64_t base = tc.split * p.out_sstride + tc.batch * p.out_bstride +
+                           static_cast<int64_t>(row0) * p.ldo + col0;
+      stage_store_f32(stg, lane, v, static_cast<float*>(p.out) + base, p.ldo, rows_valid,
+                      cols_valid);
+      if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
     } else {
       uint32_t pk[16];
       if constexpr (MODE == EPI_ACT) {
@@ -625,10 +638,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
       }
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + tc.batch * p.out_bstride +
-                         static_cast<int64_t>(row0) * p.ldo + col0;
+      const int64_t base = tc.batch * p.out_bstride + static_cast<int64_t>(row0) * p.ldo + col0;
       store_chunk_bf16(ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
-                       o, p.ldo, rows_valid, cols_valid);
+                       static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
+      if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
     }
   }
   if constexpr (MODE == EPI_DUAL) {
@@ -700,6 +713,11 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
                        y0 + col0, p.ldo, rows_valid, n_end - col0);
       store_chunk_bf16(ring, lane, uk, &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 1,
                        y1 + col0, p.ldo, rows_valid, n_end - col0);
+      if (p.visits != nullptr) {
+        const int64_t base = static_cast<int64_t>(row0) * p.ldo + col0;
+        count_writes(p, base, lane, rows_valid, n_end - col0);
+        count_writes(p, base + p.out_bstride, lane, rows_valid, n_end - col0);
+      }
       store_chunk_bf16(ring, lane, hk, &p.tmO[1], (p.tma_out & 2) != 0, col0, row0, 0,
                        hh + col0, p.ldo, rows_valid, n_end - col0);
     }

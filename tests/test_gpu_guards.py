@@ -1,18 +1,21 @@
-"""Out-of-bounds write checks (compute-sanitizer is not available): every output
-buffer and the workspace sit between guard regions filled with a sentinel byte, and
-after forward and backward (plain, fused SwiGLU, emulated exchange) the guards must be
-untouched. Shapes with ragged row and column tiles, groups that are not a multiple of
-the tile width, and co-scheduled row and column splits.
+"""Write checks standing in for a memory checker: every output buffer and the
+workspace sit between guard regions filled with a sentinel byte, which forward and
+backward (plain, fused SwiGLU, emulated exchange) must leave untouched; and debug
+write counting shows every output element of every GEMM written exactly once. Shapes
+with ragged row and column tiles, groups that are not a multiple of the tile width,
+and co-scheduled row and column splits.
 """
 
 import math
 
+import numpy as np
 import pytest
 import torch
 
 from rank_bottleneck_online_gb300 import binding as B
 from rank_bottleneck_online_gb300 import build as build_mod
 from rank_bottleneck_online_gb300 import inputs
+from rank_bottleneck_online_gb300.block import Block
 
 pytestmark = pytest.mark.gpu
 
@@ -114,3 +117,48 @@ def test_no_write_outside_the_fused_swiglu_backward_outputs():
     assert gws.intact()
     for key, g in outs.items():
         assert g.intact(), f"{key} guard overwritten"
+
+
+def _check_counts(counts, log):
+    c = counts.cpu().numpy()
+    covered = 0
+    for off, M, N, ld, planes, splits, pstride, sstride in log:
+        for sp in range(splits):
+            for pl in range(planes):
+                base = off + sp * sstride + pl * pstride
+                plane = c[base:base + (M - 1) * ld + N]
+                full = np.zeros(M * ld, dtype=c.dtype)
+                full[:plane.size] = plane
+                grid = full.reshape(M, ld)
+                assert (grid[:, :N] == 1).all(), (off, M, N, sp, pl, int(grid[:, :N].min()),
+                                                   int(grid[:, :N].max()))
+                assert (grid[:, N:] == 0).all(), (off, M, N, sp, pl)
+                covered += M * N
+    assert int(c.sum()) == covered          # nothing written outside the planes
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_every_output_element_is_written_exactly_once(case):
+    # debug write counting: each GEMM's epilogues add 1 per element they write, in a
+    # plane shaped like that GEMM's output (split-K partial planes included)
+    _, T, d, r, k, n, S, norm = case
+    w = inputs.make_block(T, d, r, k, n, has_norm=norm, seed=33)
+    blk = Block(T, d, r, k, n, S=S, has_norm=norm, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    counts = torch.zeros(160 << 20, dtype=torch.int32, device="cuda")
+    B.debug_count_writes(counts)
+    try:
+        blk.forward(x)
+        blk.backward(x, dy)
+        if k == 2:
+            B.block_fwd_swiglu(blk.desc, x, blk.gamma, blk.A, blk.B, blk.ws)
+        if d % S == 0 and (d // S) % 64 == 0:
+            B.block_fwd_btp(blk.desc, x, blk.gamma, blk.A, blk.B, blk.ws)
+        torch.cuda.synchronize()
+        log = B.debug_count_log()
+    finally:
+        B.debug_count_writes(None)
+    B.check(blk.ws)
+    # down, up, dual, dB, dA, dx per block pass, plus the fused and exchange forwards
+    assert len(log) >= 6
+    _check_counts(counts, log)
