@@ -269,8 +269,8 @@ class ClockSampler:
 
 # ------------------------------------------------------------- oracle
 
-def cpu_oracle_sample(T_sample, steps=1):
-    """Time the oracle (bf16 flow, fwd+bwd) on T_sample tokens of the workload.
+def cpu_oracle_sample(T_sample, steps=1, workload=WORKLOAD):
+    """Time the oracle (bf16 flow, fwd+bwd) on T_sample tokens of a workload.
 
     Runs in a fresh subprocess with every BLAS/OpenMP pool sized to the cores
     this process may use; returns seconds per step, tokens and thread count.
@@ -281,7 +281,7 @@ def cpu_oracle_sample(T_sample, steps=1):
         env[k] = str(cores)
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(T_sample),
-           "--_oracle-steps", str(steps)]
+           "--_oracle-steps", str(steps), "--workload", workload]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError(f"oracle sample failed: {r.stderr[-2000:]}")
@@ -290,19 +290,39 @@ def cpu_oracle_sample(T_sample, steps=1):
     return res
 
 
-def _oracle_sample_main(T_sample, steps):
+def _oracle_sample_main(T_sample, steps, workload=WORKLOAD):
     import oracle
     from rank_bottleneck_online_gb300 import inputs
 
-    c = inputs.CONFIGS[WORKLOAD]
-    w = inputs.make_inputs(WORKLOAD, T=T_sample, seed=0)
-    f = {k: inputs.as_f64(v) for k, v in w.items()}
-    args = (f["x"], f["gamma"], f["A1"], f["B1"], f["A2"], f["B2"])
+    c = inputs.CONFIGS[workload]
+    w = inputs.make_inputs(workload, T=T_sample, seed=0)
+
+    def f64(v):
+        return {k: f64(u) for k, u in v.items()} if isinstance(v, dict) else inputs.as_f64(v)
+
+    f = {k: f64(v) for k, v in w.items()}
+    S, kind = c["S"], c["kind"]
+
+    def step():
+        if kind == "mlp":
+            args = (f["x"], f["gamma"], f["A1"], f["B1"], f["A2"], f["B2"])
+            oracle.mlp_fwd(*args, S=S, flow="bf16")
+            oracle.mlp_bwd(*args, f["dout"], S=S, flow="bf16")
+        elif kind == "block":
+            args = (f["x"], f["gamma"], f["A"], f["B"])
+            oracle.block_fwd(*args, act=c["act"], S=S, flow="bf16")
+            oracle.block_bwd(*args, f["dy"], act=c["act"], S=S, flow="bf16")
+        elif kind == "layer":
+            oracle.layer_fwd(f["x"], f["p"], S=S, flow="bf16")
+            oracle.layer_bwd(f["x"], f["p"], f["dout"], f["dq"], f["dk"], S=S, flow="bf16")
+        else:
+            oracle.svd_pair_fwd(f["x"], f["p"], S=S, flow="bf16")
+            oracle.svd_pair_bwd(f["x"], f["p"], f["dy_qkv"], f["dy_gu"], S=S, flow="bf16")
+
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        oracle.mlp_fwd(*args, S=c["S"], flow="bf16")
-        oracle.mlp_bwd(*args, f["dout"], S=c["S"], flow="bf16")
+        step()
         times.append(time.perf_counter() - t0)
     print(json.dumps({"seconds": times, "tokens": T_sample}))
 
@@ -679,12 +699,14 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     gpu_launches = sum(prof_kernels.get(k, v[0]) for k, v in prof.items())
 
     cpu = None
-    if world == 1 and not args.skip_aux and default:
+    if world == 1 and not args.skip_aux:
+        # the wide workloads (13B layer, 40B pair) on 512 sampled tokens, the rest on 1024
+        t_s = CPU_SAMPLE_T if _cfg(args.workload)["d"] <= 4096 else CPU_SAMPLE_T // 2
         try:
-            res = cpu_oracle_sample(CPU_SAMPLE_T, steps=1)
-            cpu = {"value": CPU_SAMPLE_T / res["seconds"][0], "unit": "tokens/s",
+            res = cpu_oracle_sample(t_s, steps=1, workload=args.workload)
+            cpu = {"value": t_s / res["seconds"][0], "unit": "tokens/s",
                    "cores": res["cores"], "kind": "oracle",
-                   "sample": f"{CPU_SAMPLE_T} of {T} tokens of {WORKLOAD} (full d/r/ffn), "
+                   "sample": f"{t_s} of {T} tokens of {args.workload} (full widths), "
                              "oracle bf16 flow fwd+bwd in numpy fp64, one run"}
         except Exception as ex:  # noqa: BLE001
             cpu = {"value": None, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
@@ -755,7 +777,7 @@ def main(argv=None):
     ap.add_argument("--_oracle-steps", type=int, default=1, dest="oracle_steps")
     args = ap.parse_args(argv)
     if args.oracle_sample:
-        _oracle_sample_main(args.oracle_sample, args.oracle_steps)
+        _oracle_sample_main(args.oracle_sample, args.oracle_steps, args.workload)
         return 0
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
