@@ -169,7 +169,7 @@ struct Plan {
   int n_cols_dual;                  // rows of K4's q partials (column tiles x halves)
   int n_cols_wA;                    // rows of K6's dgamma partials (column tiles x halves)
   int splits_B, kbps_B, splits_A, kbps_A;
-  size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_part, total;
+  size_t off_rstd, off_ssq, off_Ap, off_a, off_dzs, off_q, off_dg, off_partB, off_partA, total;
 };
 
 // Split-K choice for a weight gradient: minimise the estimated time
@@ -258,7 +258,9 @@ Plan make_plan(const boost_block_desc& D, int sms) {
   P.off_dg = off;   off = align_up(off + sizeof(float) * P.n_cols_wA * D.d);
   const size_t partB = P.splits_B > 1 ? sizeof(float) * P.splits_B * D.k * D.r * D.n : 0;
   const size_t partA = P.splits_A > 1 ? sizeof(float) * P.splits_A * D.d * P.kr : 0;
-  P.off_part = off; off = align_up(off + std::max(partA, partB));
+  // separate regions: dB and dA may run concurrently (on two streams)
+  P.off_partB = off; off = align_up(off + partB);
+  P.off_partA = off; off = align_up(off + partA);
   P.total = off;
   return P;
 }
@@ -520,6 +522,76 @@ cudaError_t launch_gemm_cols(const Shape& sh, int mode, const GemmParams& g_in, 
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, cs->join, 0);
   return e;
 }
+
+// The three backward GEMMs that follow the dual kernel (dB, dA, dx) depend only on its
+// outputs, not on each other: dB and dA go to two more streams forked from the
+// caller's stream, dx stays on it, and everything joins back before the call returns.
+// Each persistent GEMM fills the GPU on its own; running them concurrently lets one's
+// last, partly filled wave overlap the next one's start. BOOST_BWD_STREAMS=0 turns it
+// off. Per-device streams and events, created on first use; one fork/join at a time.
+struct BwdStreams {
+  cudaStream_t aux[2] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
+  bool ok = false;
+  std::mutex order;
+};
+
+BwdStreams* bwd_streams() {
+  static BwdStreams bs[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  BwdStreams& b = bs[dev];
+  if (!b.ok) {
+    for (int i = 0; i < 2; ++i)
+      if (cudaStreamCreateWithFlags(&b.aux[i], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&b.join[i], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+      }
+    if (cudaEventCreateWithFlags(&b.fork, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    b.ok = true;
+  }
+  return &b;
+}
+
+class BwdFork {
+ public:
+  explicit BwdFork(cudaStream_t s) : s_(s) {
+    static const int on = env_int("BOOST_BWD_STREAMS", 1);
+    if (!on || (bs_ = bwd_streams()) == nullptr) return;
+    lk_ = std::unique_lock<std::mutex>(bs_->order);
+    if (cudaEventRecord(bs_->fork, s_) != cudaSuccess ||
+        cudaStreamWaitEvent(bs_->aux[0], bs_->fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(bs_->aux[1], bs_->fork, 0) != cudaSuccess) {
+      cudaGetLastError();
+      bs_ = nullptr;
+      lk_.unlock();
+    }
+  }
+  ~BwdFork() {   // join on every exit path, so the caller's stream orders all of it
+    if (bs_ == nullptr) return;
+    for (int i = 0; i < 2; ++i) {
+      cudaEventRecord(bs_->join[i], bs_->aux[i]);
+      cudaStreamWaitEvent(s_, bs_->join[i], 0);
+    }
+  }
+  BwdFork(const BwdFork&) = delete;
+  BwdFork& operator=(const BwdFork&) = delete;
+  cudaStream_t stream(int i) const { return bs_ != nullptr ? bs_->aux[i] : s_; }
+
+ private:
+  cudaStream_t s_;
+  BwdStreams* bs_ = nullptr;
+  std::unique_lock<std::mutex> lk_;
+};
 
 }  // namespace
 
@@ -865,7 +937,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
-  float* part = ws_at<float>(ws, P.off_part);
+  BwdFork fork(s);
   const double wB_flops = 2.0 * P.T * P.kr * P.n;
   const double wB_bytes = 2.0 * (P.T * P.kr + P.k * P.T * P.n + P.kr * P.n);
   const double wA_flops = 2.0 * P.T * P.d * P.kr;
@@ -874,6 +946,8 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
 
   // K5: dB[i] = a[:, group i]^T @ dy[i]  (M = r, N = n, K = T).
   {
+    const cudaStream_t sb = fork.stream(0);
+    float* part = ws_at<float>(ws, P.off_partB);
     GemmParams w = base_params(P, err);
     if (!make_map(&w.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, 64)) return BOOST_ERR_CUDA;
     if (!make_map(&w.tmB[0], dy, P.n, P.T, P.k, P.n * 2, P.T * P.n * 2, 64, 64, 1))
@@ -894,23 +968,25 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.out = part;
       w.out_sstride = P.k * P.r * P.n;
       {
-        ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-        e = launch_gemm_cols(P.wB, EPI_F32, w, sms, s);
+        ProfScope ps(sb, K_WGRAD_B, wB_flops, wB_bytes);
+        e = launch_gemm_cols(P.wB, EPI_F32, w, sms, sb);
       }
       if (e == cudaSuccess) {
-        ProfScope ps(s, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
-        e = launch_splitk_sum_bf16(part, P.splits_B, P.k * P.r * P.n, dB, s);
+        ProfScope ps(sb, K_SPLITK_SUM, 0.0, (4.0 * P.splits_B + 2.0) * P.kr * P.n);
+        e = launch_splitk_sum_bf16(part, P.splits_B, P.k * P.r * P.n, dB, sb);
       }
     } else {
       w.out = dB;
-      ProfScope ps(s, K_WGRAD_B, wB_flops, wB_bytes);
-      e = launch_gemm_cols(P.wB, EPI_BF16, w, sms, s);
+      ProfScope ps(sb, K_WGRAD_B, wB_flops, wB_bytes);
+      e = launch_gemm_cols(P.wB, EPI_BF16, w, sms, sb);
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
   }
 
   // K6: G = x^T @ dzs (M = d, N = k*r, K = T); dA = gamma (.) G, dgamma = rowsum(A (.) G).
   {
+    const cudaStream_t sa = fork.stream(1);
+    float* part = ws_at<float>(ws, P.off_partA);
     GemmParams w = base_params(P, err);
     if (!map_2d(&w.tmA[0], x, P.T, P.d, 64, 64)) return BOOST_ERR_CUDA;
     if (!map_2d(&w.tmB[0], dzs, P.T, P.kr, 64, 64)) return BOOST_ERR_CUDA;
@@ -928,13 +1004,13 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.out = part;
       w.out_sstride = P.d * P.kr;
       {
-        ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm_cols(P.wA, EPI_F32, w, sms, s);
+        ProfScope ps(sa, K_WGRAD_A, wA_flops, wA_bytes);
+        e = launch_gemm_cols(P.wA, EPI_F32, w, sms, sa);
       }
       if (e == cudaSuccess) {
-        ProfScope ps(s, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
+        ProfScope ps(sa, K_FINALIZE_DA, 0.0, (4.0 * P.splits_A + 4.0) * P.d * P.kr + 4.0 * P.d);
         e = launch_splitk_finalize_dA(part, P.splits_A, P.d, P.kr, D.has_norm ? gamma : nullptr,
-                                      A, dA, D.has_norm ? dgamma : nullptr, s);
+                                      A, dA, D.has_norm ? dgamma : nullptr, sa);
       }
     } else {
       w.out = dA;
@@ -942,12 +1018,12 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.wA = D.has_norm ? static_cast<const __nv_bfloat16*>(A) : nullptr;
       w.dgpart = D.has_norm ? ws_at<float>(ws, P.off_dg) : nullptr;
       {
-        ProfScope ps(s, K_WGRAD_A, wA_flops, wA_bytes);
-        e = launch_gemm_cols(P.wA, EPI_DA, w, sms, s);
+        ProfScope ps(sa, K_WGRAD_A, wA_flops, wA_bytes);
+        e = launch_gemm_cols(P.wA, EPI_DA, w, sms, sa);
       }
       if (e == cudaSuccess && D.has_norm) {
-        ProfScope ps(s, K_DGAMMA, 0.0, 4.0 * P.n_cols_wA * P.d + 2.0 * P.d);
-        e = launch_dgamma_reduce(ws_at<float>(ws, P.off_dg), P.n_cols_wA, P.d, dgamma, s);
+        ProfScope ps(sa, K_DGAMMA, 0.0, 4.0 * P.n_cols_wA * P.d + 2.0 * P.d);
+        e = launch_dgamma_reduce(ws_at<float>(ws, P.off_dg), P.n_cols_wA, P.d, dgamma, sa);
       }
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
