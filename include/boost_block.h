@@ -25,12 +25,13 @@
  *   process, created on first use: a second stream and two events that let one
  *   GEMM run as two concurrent launches over disjoint rows or columns
  *   ("co-scheduling": a launch of 8-CTA clusters plus a CTA-pair launch on the
- *   SMs no cluster fits), and cached cluster-occupancy counts
- *   (boost_rmsnorm_rstd_noalloc adds its fixed array, below).
+ *   SMs no cluster fits); two more streams and three events on which the backward
+ *   runs its dB and dA GEMMs concurrently with dx; and cached cluster-occupancy
+ *   counts (boost_rmsnorm_rstd_noalloc adds its fixed array, below).
  * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
- *   stream): a co-scheduled GEMM forks from `stream` to the side stream and joins
- *   back with events, so everything a call enqueues is ordered after earlier
- *   work on `stream` and before later work on it. Calls may be captured into
+ *   stream): work on the library's other streams is forked from `stream` and
+ *   joined back to it with events, so everything a call enqueues is ordered after
+ *   earlier work on `stream` and before later work on it. Calls may be captured into
  *   CUDA graphs (the fork and join become part of the capture). Every argument
  *   is validated on the host before anything is enqueued: a call that returns
  *   BOOST_ERR_INVALID_ARG, _UNSUPPORTED_SHAPE, _ALIGNMENT or _WORKSPACE has
@@ -41,9 +42,9 @@
  * - Errors found on the device (a bounded wait that ran out) are recorded in
  *   the workspace's error word and reported by boost_block_check().
  * - Thread safety: calls on different workspaces may run concurrently; the
- *   fork/launch/join sequences on the shared side stream are serialised
+ *   fork/launch/join sequences on the library's streams are serialised
  *   internally. Two threads capturing graphs on different streams at the same
- *   time would both capture the side stream: do not overlap such captures.
+ *   time would both capture those streams: do not overlap such captures.
  */
 #ifndef BOOST_BLOCK_H
 #define BOOST_BLOCK_H
