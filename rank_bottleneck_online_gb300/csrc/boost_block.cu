@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -523,21 +524,22 @@ cudaError_t launch_gemm_cols(const Shape& sh, int mode, const GemmParams& g_in, 
   return e;
 }
 
-// The three backward GEMMs that follow the dual kernel (dB, dA, dx) depend only on its
-// outputs, not on each other: dB and dA go to two more streams forked from the
-// caller's stream, dx stays on it, and everything joins back before the call returns.
+// Independent steps of one call run on two more streams forked from the caller's stream
+// and joined back to it (on every exit path) before the call returns: the three
+// backward GEMMs after the dual kernel (dB and dA on the extra streams, dx on the
+// caller's), and the statistics and the gamma fold before a normed block's GEMMs.
 // Each persistent GEMM fills the GPU on its own; running them concurrently lets one's
-// last, partly filled wave overlap the next one's start. BOOST_BWD_STREAMS=0 turns it
+// last, partly filled wave overlap the next one's start. BOOST_FORK_STREAMS=0 turns it
 // off. Per-device streams and events, created on first use; one fork/join at a time.
-struct BwdStreams {
+struct ForkStreams {
   cudaStream_t aux[2] = {nullptr, nullptr};
   cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
   bool ok = false;
   std::mutex order;
 };
 
-BwdStreams* bwd_streams() {
-  static BwdStreams bs[64];
+ForkStreams* fork_streams() {
+  static ForkStreams bs[64];
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -545,7 +547,7 @@ BwdStreams* bwd_streams() {
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(mu);
-  BwdStreams& b = bs[dev];
+  ForkStreams& b = bs[dev];
   if (!b.ok) {
     for (int i = 0; i < 2; ++i)
       if (cudaStreamCreateWithFlags(&b.aux[i], cudaStreamNonBlocking) != cudaSuccess ||
@@ -562,11 +564,11 @@ BwdStreams* bwd_streams() {
   return &b;
 }
 
-class BwdFork {
+class StreamFork {
  public:
-  explicit BwdFork(cudaStream_t s) : s_(s) {
-    static const int on = env_int("BOOST_BWD_STREAMS", 1);
-    if (!on || (bs_ = bwd_streams()) == nullptr) return;
+  explicit StreamFork(cudaStream_t s) : s_(s) {
+    static const int on = env_int("BOOST_FORK_STREAMS", 1);
+    if (!on || (bs_ = fork_streams()) == nullptr) return;
     lk_ = std::unique_lock<std::mutex>(bs_->order);
     if (cudaEventRecord(bs_->fork, s_) != cudaSuccess ||
         cudaStreamWaitEvent(bs_->aux[0], bs_->fork, 0) != cudaSuccess ||
@@ -576,20 +578,20 @@ class BwdFork {
       lk_.unlock();
     }
   }
-  ~BwdFork() {   // join on every exit path, so the caller's stream orders all of it
+  ~StreamFork() {   // join on every exit path, so the caller's stream orders all of it
     if (bs_ == nullptr) return;
     for (int i = 0; i < 2; ++i) {
       cudaEventRecord(bs_->join[i], bs_->aux[i]);
       cudaStreamWaitEvent(s_, bs_->join[i], 0);
     }
   }
-  BwdFork(const BwdFork&) = delete;
-  BwdFork& operator=(const BwdFork&) = delete;
+  StreamFork(const StreamFork&) = delete;
+  StreamFork& operator=(const StreamFork&) = delete;
   cudaStream_t stream(int i) const { return bs_ != nullptr ? bs_->aux[i] : s_; }
 
  private:
   cudaStream_t s_;
-  BwdStreams* bs_ = nullptr;
+  ForkStreams* bs_ = nullptr;
   std::unique_lock<std::mutex> lk_;
 };
 
@@ -741,6 +743,7 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
   if (D.has_norm) {
     rs = rstd ? rstd : ws_at<float>(ws, P.off_rstd);
     cudaError_t e;
+    StreamFork fork(s);   // the fold runs beside the statistics
     {
       // (under the emulated exchange the shard sums of squares go into the payload; the
       // row scale is formed again after the reduction, from the exchanged sums)
@@ -751,12 +754,12 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
     {
-      ProfScope ps(s, K_FOLD, 0.0, fold_bytes(P));
-      e = launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s);
+      ProfScope ps(fork.stream(0), K_FOLD, 0.0, fold_bytes(P));
+      e = launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, fork.stream(0));
     }
     if (e != cudaSuccess) return BOOST_ERR_CUDA;
     Ap = ws_at<void>(ws, P.off_Ap);
-  }
+  }   // joined: the down-projection needs both
   void* a = ws_at<void>(ws, P.off_a);
 
   GemmParams g = base_params(P, err);
@@ -888,7 +891,11 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
   const void* Ap = A;
   const float* rs = nullptr;
   if (D.has_norm) {
+    std::unique_ptr<StreamFork> fork;   // the fold beside the statistics, when both run
+    cudaStream_t sf = s;
     if (rstd == nullptr) {
+      fork = std::make_unique<StreamFork>(s);
+      sf = fork->stream(0);
       float* r = ws_at<float>(ws, P.off_rstd);
       ProfScope ps(s, K_STATS, 0.0, stats_bytes(P, D.S));
       if (launch_rmsnorm_stats(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq), r, s) !=
@@ -899,12 +906,12 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       rs = rstd;
     }
     {
-      ProfScope ps(s, K_FOLD, 0.0, fold_bytes(P));
-      if (launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, s) != cudaSuccess)
+      ProfScope ps(sf, K_FOLD, 0.0, fold_bytes(P));
+      if (launch_fold_gamma(gamma, A, ws_at<void>(ws, P.off_Ap), D.d, P.kr, sf) != cudaSuccess)
         return BOOST_ERR_CUDA;
     }
     Ap = ws_at<void>(ws, P.off_Ap);
-  }
+  }   // joined before the dual kernel
   void* a = ws_at<void>(ws, P.off_a);
   void* dzs = ws_at<void>(ws, P.off_dzs);
   float* qpart = ws_at<float>(ws, P.off_q);
@@ -937,7 +944,7 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
-  BwdFork fork(s);
+  StreamFork fork(s);
   const double wB_flops = 2.0 * P.T * P.kr * P.n;
   const double wB_bytes = 2.0 * (P.T * P.kr + P.k * P.T * P.n + P.kr * P.n);
   const double wA_flops = 2.0 * P.T * P.d * P.kr;
