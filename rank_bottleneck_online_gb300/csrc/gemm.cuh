@@ -9,7 +9,9 @@
 //                    commits the stage / accumulator barriers
 //   warps 2..9     : epilogue; tcgen05.ld of the accumulator (two warps per TMEM lane
 //                    quarter taking alternate 32-column chunks, one output row per
-//                    thread), fused math, global stores
+//                    thread), fused math, stores through per-warp shared-memory
+//                    staging (coalesced plain stores, or TMA bulk stores in the SwiGLU
+//                    modes), epilogue inputs (x, gate, up) streamed in by TMA
 // CG = 2 runs each tile on a CTA pair (a cluster of two SMs, tcgen05 cta_group::2):
 // each SM stages its own 128 rows of A and half of the BN rows of B, so the operand
 // bytes each SM moves per MMA flop are 2/3 of the single-SM tile's. The even CTA
@@ -22,7 +24,11 @@
 // MCM = MCN = 2 half of the L2->SM bytes per MMA flop. A stage is refilled once every
 // pair of the cluster has released it.
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
-// mainloop of tile i+1. Every mbarrier wait is bounded (ptx.cuh).
+// mainloop of tile i+1, except with two 256-column accumulators per tile (EPI_DUAL,
+// EPI_UPGLU), which fill TMEM; EPI_UPGLU then frees its first accumulator as soon as
+// it has been read. A launch may cover a row range (m_base, m_extent) or start at a
+// column (n_base) of the output, so that two launches of different cluster shapes can
+// share one GEMM. Every mbarrier wait is bounded (ptx.cuh).
 //
 // Operands are described by "views" of 3-D tensor maps: which map dimension
 // carries the MN index, which the K index and which the batch index, and whether
