@@ -665,11 +665,12 @@ def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
     return max_over_ranks(time.perf_counter() - t0, dist, dev)
 
 
-# Operations the library runs on its forked streams, concurrently with other GEMMs
-# (unless BOOST_FORK_STREAMS=0): their event intervals include time shared with the
-# concurrent GEMMs, so they are not kernel durations.
-FORKED_OPS = ("gemm_wgrad_B", "gemm_wgrad_A", "splitk_sum", "splitk_finalize_dA",
-              "dgamma_reduce", "fold_gamma")
+# Operations the library runs concurrently with other GEMMs (unless BOOST_FORK_STREAMS=0):
+# dB and dA on forked streams beside dx on the caller's stream, the gamma fold beside
+# the statistics. Their event intervals include time shared with the concurrent work,
+# so they are not kernel durations.
+OVERLAPPED_OPS = ("gemm_wgrad_B", "gemm_wgrad_A", "splitk_sum", "splitk_finalize_dA",
+                  "dgamma_reduce", "gemm_dx", "gemm_dx_swiglu", "fold_gamma", "rmsnorm_stats")
 
 
 def _forked():
@@ -686,7 +687,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     peaks = load_peaks()
     # dominant kernel: the largest share of the timed region among the operations timed
     # alone on the caller's stream (a forked operation's interval is not its duration)
-    overlapped = set(FORKED_OPS) if _forked() else set()
+    overlapped = set(OVERLAPPED_OPS) if _forked() else set()
     serial = {k: v for k, v in prof.items() if k not in overlapped} or prof
     name, (launches, kms, kfl, kby) = max(serial.items(), key=lambda kv: kv[1][1])
     bound = "tensor" if kfl > 0 else "hbm"
