@@ -677,6 +677,13 @@ def _forked():
     return os.environ.get("BOOST_FORK_STREAMS", "1") != "0"
 
 
+def dominant_kernel(prof, overlapped):
+    """(name, (launches, ms, flops, bytes)) of the operation with the largest event time
+    among those that run alone (not in `overlapped`); all of them if none does."""
+    serial = {k: v for k, v in prof.items() if k not in overlapped} or prof
+    return max(serial.items(), key=lambda kv: kv[1][1])
+
+
 def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn,
             S, btp=None, dense=None, cuts=None):
     ms_step = ms_total / args.steps
@@ -688,8 +695,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     # dominant kernel: the largest share of the timed region among the operations timed
     # alone on the caller's stream (a forked operation's interval is not its duration)
     overlapped = set(OVERLAPPED_OPS) if _forked() else set()
-    serial = {k: v for k, v in prof.items() if k not in overlapped} or prof
-    name, (launches, kms, kfl, kby) = max(serial.items(), key=lambda kv: kv[1][1])
+    name, (launches, kms, kfl, kby) = dominant_kernel(prof, overlapped)
     bound = "tensor" if kfl > 0 else "hbm"
     if bound == "tensor":
         achieved = kfl / (kms / 1e3) / 1e12

@@ -106,3 +106,15 @@ def test_workload_flop_model():
     d, r, f = 5120, 1280, 13824
     assert lay == sum(8 * di * kr + 6 * kr * n for di, kr, n in
                       [(d, 3 * r, d), (d, r, d), (d, 2 * r, f), (f, r, d)])
+
+
+def test_dominant_kernel_skips_overlapped_operations():
+    # an overlapped operation's event interval includes time shared with its concurrent
+    # siblings, so it is never named the dominant kernel while a serial one exists
+    prof = {"gemm_wgrad_B": (2, 9.0, 1e12, 1e9), "gemm_dual": (2, 5.0, 2e12, 1e9),
+            "gemm_down_act": (2, 3.0, 1e12, 1e9)}
+    name, _ = bench.dominant_kernel(prof, set(bench.OVERLAPPED_OPS))
+    assert name == "gemm_dual"
+    assert bench.dominant_kernel(prof, set())[0] == "gemm_wgrad_B"
+    only = {"gemm_wgrad_B": (1, 1.0, 1.0, 1.0)}
+    assert bench.dominant_kernel(only, set(bench.OVERLAPPED_OPS))[0] == "gemm_wgrad_B"
