@@ -32,13 +32,13 @@ int gemm_resident_bwd(int bn, int mode, int cg, int mcm, int mcn, int num_sms);
 
 cudaError_t launch_gemm(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
-  if (mode == EPI_ACT || mode == EPI_BF16 || mode == EPI_UPGLU)
+  if (mode == EPI_ACT || mode == EPI_BF16 || mode == EPI_UPGLU || mode == EPI_BF16T)
     return launch_gemm_fwd_modes(bn, mode, cg, mcm, mcn, p, num_sms, stream);
   return launch_gemm_bwd_modes(bn, mode, cg, mcm, mcn, p, num_sms, stream);
 }
 
 int gemm_resident(int bn, int mode, int cg, int mcm, int mcn, int num_sms) {
-  if (mode == EPI_ACT || mode == EPI_BF16 || mode == EPI_UPGLU)
+  if (mode == EPI_ACT || mode == EPI_BF16 || mode == EPI_UPGLU || mode == EPI_BF16T)
     return gemm_resident_fwd(bn, mode, cg, mcm, mcn, num_sms);
   return gemm_resident_bwd(bn, mode, cg, mcm, mcn, num_sms);
 }
@@ -695,9 +695,13 @@ cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n + P.T * P.n));
     e = launch_gemm_rows(P.up, EPI_UPGLU, u, sms, s);
   } else {
+    // with a short K the epilogue's stores weigh most: store them through TMA
+    static const int tma_up_max_r = env_int("BOOST_TMA_UP_MAX_R", 512);
+    const bool tma = P.r <= tma_up_max_r;
+    if (tma) set_out_maps(u, P.T, P.n, P.k);
     ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
-    e = launch_gemm_rows(P.up, EPI_BF16, u, sms, s);
+    e = launch_gemm_rows(P.up, tma ? EPI_BF16T : EPI_BF16, u, sms, s);
   }
   return e;
 }

@@ -62,6 +62,8 @@ enum EpiMode : int {
   EPI_GLU = 6,     // dh = bf16(acc); out = dh*up*silu'(gate), out2 = dh*silu(gate) (SwiGLU bwd)
   EPI_UPGLU = 7,   // two accumulators: gate, up = bf16(acc0), bf16(acc1) to out[0], out[1];
                    // out2 = h = bf16(silu(gate) * up)     (up-projection + SwiGLU fwd)
+  EPI_BF16T = 8,   // EPI_BF16 through TMA stores (short-K up-projections, where the
+                   // epilogue's stores weigh most)
 };
 
 struct OperandView {
@@ -132,7 +134,7 @@ struct GemmCfg {
   // pays where the epilogue is the bottleneck (the SwiGLU epilogues); elsewhere they
   // compete with the operand loads for the SM's TMA unit, and plain coalesced stores
   // through the warp's staging block measured faster.
-  static constexpr bool kTmaStore = (MODE == EPI_GLU || MODE == EPI_UPGLU);
+  static constexpr bool kTmaStore = (MODE == EPI_GLU || MODE == EPI_UPGLU || MODE == EPI_BF16T);
   // Epilogue inputs streamed by TMA (EpiLoader): gate and up for EPI_GLU, x for EPI_DX,
   // kEpiDepth chunks ahead of the consumer. One chunk ahead measured faster than two:
   // the shared memory a second slot takes costs the mainloop a pipeline stage, and these
@@ -565,7 +567,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act),
                               act_fwd(s_row * v[2 * i + 1], p.act));
-      } else if constexpr (MODE == EPI_BF16) {
+      } else if constexpr (MODE == EPI_BF16 || MODE == EPI_BF16T) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
       } else if constexpr (MODE == EPI_DUAL) {
