@@ -259,3 +259,54 @@ def test_forward_backward_replay_from_a_cuda_graph():
     B.check(blk.ws)
     for a, b in zip(eager, (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma)):
         assert torch.equal(a, b)
+
+
+def test_two_host_threads_on_their_own_streams_match_serial_runs():
+    # calls on different workspaces may run concurrently: the library's shared fork
+    # and co-scheduling streams are used one fork/join sequence at a time
+    import threading
+
+    shape = (4352, 512, 512, 2, 1024, 4)          # co-scheduled rows and forked backward
+    blocks, data = [], []
+    for seed in (41, 42):
+        T, d, r, k, n, S = shape
+        w = inputs.make_block(T, d, r, k, n, seed=seed)
+        blocks.append(Block(T, d, r, k, n, S=S, weights=w))
+        data.append((w["x"].cuda(), w["dy"].cuda()))
+
+    def outputs(blk):
+        return [t.clone() for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma)]
+
+    serial = []
+    for blk, (x, dy) in zip(blocks, data):
+        blk.forward(x)
+        blk.backward(x, dy)
+        torch.cuda.synchronize()
+        serial.append(outputs(blk))
+        for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma):
+            t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    blocks[i].forward(data[i][0])
+                    blocks[i].backward(*data[i])
+            s.synchronize()
+        except Exception as ex:  # noqa: BLE001
+            errors.append(ex)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for blk, want in zip(blocks, serial):
+        B.check(blk.ws)
+        for a, b in zip(outputs(blk), want):
+            assert torch.equal(a, b)
