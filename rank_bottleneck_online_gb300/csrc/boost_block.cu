@@ -691,6 +691,8 @@ cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void
     u.tmB[1] = u.tmB[0];
     u.out2 = h;
     set_out_maps(u, P.T, P.n, 2, 1);
+    // the fused epilogue stores gate, up and h only through these maps
+    if (u.tma_out != 3) return cudaErrorInvalidValue;
     ProfScope ps(s, K_UP_GLU, 2.0 * P.T * P.kr * P.n,
                  2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n + P.T * P.n));
     e = launch_gemm_rows(P.up, EPI_UPGLU, u, sms, s);

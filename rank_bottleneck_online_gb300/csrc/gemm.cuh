@@ -671,63 +671,91 @@ __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoid
 // [row0, row0 + 32), columns [n0, n_end), the 32-column chunks half, half + kEpiHalves,
 // ...). Accumulator 0 (gate, TMEM columns [0, BN)) is read first and kept in registers
 // as bf16; then, if `release0` is set, this warp's arrival on it lets the MMA warp start
-// the next tile's gate segment while accumulator 1 (up, columns [BN, 2 BN)) is read and
-// gate, up and h = silu(gate) * up are stored chunk by chunk.
+// the next tile's gate segment. Accumulator 1 (up, columns [BN, 2 BN)) is read next,
+// also kept as bf16, and `release1` frees it (or the whole accumulator set) before any
+// store: the next tile's MMAs then overlap all of this tile's gate, up and
+// h = silu(gate) * up stores. Gate and up of the warp's columns take 128 registers a
+// thread, so the TMEM loads are 16 columns wide to keep the transient small. The stores
+// go through the output maps only (the launch requires both).
 template <int BN, int CG, int kSlots, bool kTma>
 __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0, int32_t n0,
                                                int32_t n_end, uint32_t t_row,
                                                StoreRing<kSlots, kTma>& ring, int lane, int half,
-                                               uint64_t* release0, uint32_t leader_rank) {
+                                               uint64_t* release0, uint64_t* release1,
+                                               uint32_t leader_rank) {
   constexpr int kChunks = BN / 32 / kEpiHalves;
   const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
   __nv_bfloat16* y0 = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row0) * p.ldo;
   __nv_bfloat16* y1 = y0 + p.out_bstride;
   __nv_bfloat16* hh = static_cast<__nv_bfloat16*>(p.out2) + static_cast<int64_t>(row0) * p.ldo;
-  uint32_t gk[kChunks][16];
-#pragma unroll
-  for (int j = 0; j < kChunks; ++j) {
-    const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
-    if (col0 < n_end) {                     // warp-uniform
-      float v[32];
-      tmem_ld_32x32b_x32(t_row + (half + j * kEpiHalves) * 32, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) gk[j][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-    }
-  }
-  if (release0 != nullptr) {
+  auto release = [&](uint64_t* bar) {
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(release0), leader_rank));
-      else mbar_arrive(release0);
+      if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(bar), leader_rank));
+      else mbar_arrive(bar);
+    }
+  };
+  uint32_t gk[kChunks][16];
+  uint32_t uk[kChunks][16];
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int c = half + j * kEpiHalves;
+    if (n0 + c * 32 < n_end) {              // warp-uniform
+#pragma unroll
+      for (int hh16 = 0; hh16 < 2; ++hh16) {
+        float v[16];
+        tmem_ld_32x32b_x16(t_row + c * 32 + hh16 * 16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gk[j][hh16 * 8 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      }
     }
   }
+  if (release0 != nullptr) release(release0);
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int c = half + j * kEpiHalves;
+    if (n0 + c * 32 < n_end) {              // warp-uniform
+#pragma unroll
+      for (int hh16 = 0; hh16 < 2; ++hh16) {   // 16 columns per load: fewer live registers
+        float w[16];
+        tmem_ld_32x32b_x16(t_row + BN + c * 32 + hh16 * 16, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) uk[j][hh16 * 8 + i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
+      }
+    }
+  }
+  release(release1);
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) {
     const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
     if (col0 < n_end) {                     // warp-uniform
-      float w[32];
-      tmem_ld_32x32b_x32(t_row + BN + (half + j * kEpiHalves) * 32, w);
-      tmem_ld_wait();
-      uint32_t uk[16], hk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        uk[i] = pack_bf16x2(w[2 * i], w[2 * i + 1]);
-        hk[i] = pack_bf16x2(swiglu_h(bf16_lo(gk[j][i]), bf16_lo(uk[i])),
-                            swiglu_h(bf16_hi(gk[j][i]), bf16_hi(uk[i])));
-      }
-      store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 0,
+      store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], true, col0, row0, 0,
                        y0 + col0, p.ldo, rows_valid, n_end - col0);
-      store_chunk_bf16(ring, lane, uk, &p.tmO[0], (p.tma_out & 1) != 0, col0, row0, 1,
+      store_chunk_bf16(ring, lane, uk[j], &p.tmO[0], true, col0, row0, 1,
                        y1 + col0, p.ldo, rows_valid, n_end - col0);
-      if (p.visits != nullptr) {
+      // h after gate and up have gone to shared memory, in place of this chunk's gate
+      // registers (the live set stays at gate + up)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        gk[j][i] = pack_bf16x2(swiglu_h(bf16_lo(gk[j][i]), bf16_lo(uk[j][i])),
+                               swiglu_h(bf16_hi(gk[j][i]), bf16_hi(uk[j][i])));
+      const uint32_t (&hk)[16] = gk[j];
+      store_chunk_bf16(ring, lane, hk, &p.tmO[1], true, col0, row0, 0,
+                       hh + col0, p.ldo, rows_valid, n_end - col0);
+    }
+  }
+  if (p.visits != nullptr) {                // debug write counting (gate and up)
+#pragma unroll 1
+    for (int j = 0; j < kChunks; ++j) {
+      const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
+      if (col0 < n_end) {
         const int64_t base = static_cast<int64_t>(row0) * p.ldo + col0;
         count_writes(p, base, lane, rows_valid, n_end - col0);
         count_writes(p, base + p.out_bstride, lane, rows_valid, n_end - col0);
       }
-      store_chunk_bf16(ring, lane, hk, &p.tmO[1], (p.tma_out & 2) != 0, col0, row0, 0,
-                       hh + col0, p.ldo, rows_valid, n_end - col0);
     }
   }
 }
@@ -1011,18 +1039,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if constexpr (MODE == EPI_UPGLU) {
         epilogue_upglu<BN, CG, Cfg::kStoreSlots, Cfg::kTmaStore>(
             p, row0, pn0, pend, t_row, ring, lane, half,
-            Cfg::kSplitRelease ? &tempty_bar[0] : nullptr, leader_rank);
+            Cfg::kSplitRelease ? &tempty_bar[0] : nullptr,
+            &tempty_bar[Cfg::kSplitRelease ? 1 : acc], leader_rank);
       } else {
         epilogue_tile<BN, MODE, Cfg::kStoreSlots, Cfg::kTmaStore>(
             p, tc, row0, pn0, pend, t_row, stg, ring, ld, lane,
             tc.n_blk * MCN + static_cast<int32_t>(pn), half);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        uint64_t* bar = &tempty_bar[Cfg::kSplitRelease ? 1 : acc];
-        if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(bar), leader_rank));
-        else mbar_arrive(bar);
+      if constexpr (MODE != EPI_UPGLU) {   // (the SwiGLU epilogue released its own)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          uint64_t* bar = &tempty_bar[acc];
+          if constexpr (CG == 2) mbar_arrive_cluster(mapa_shared(smem_u32(bar), leader_rank));
+          else mbar_arrive(bar);
+        }
       }
       if (++acc == Cfg::kAccStages) {
         acc = 0;
