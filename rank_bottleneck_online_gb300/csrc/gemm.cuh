@@ -25,8 +25,8 @@
 // pair of the cluster has released it.
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
 // mainloop of tile i+1, except with two 256-column accumulators per tile (EPI_DUAL,
-// EPI_UPGLU), which fill TMEM; EPI_UPGLU then frees its first accumulator as soon as
-// it has been read. A launch may cover a row range (m_base, m_extent) or start at a
+// EPI_UPGLU), which fill TMEM; EPI_UPGLU then frees each accumulator as soon as it
+// has been read into registers, before its stores. A launch may cover a row range (m_base, m_extent) or start at a
 // column (n_base) of the output, so that two launches of different cluster shapes can
 // share one GEMM. Every mbarrier wait is bounded (ptx.cuh).
 //
