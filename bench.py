@@ -374,6 +374,19 @@ def max_over_ranks(value, dist=None, device="cpu"):
     return float(t.item())
 
 
+def step_spread(ms):
+    """Median and spread of per-step device times (ms), from events recorded between
+    the timed steps; nearest-rank percentiles."""
+    if not ms:
+        return None
+    v = sorted(ms)
+    n = len(v)
+    pick = lambda q: v[min(n - 1, max(0, int(round(q * (n - 1)))))]  # noqa: E731
+    med = v[n // 2] if n % 2 else 0.5 * (v[n // 2 - 1] + v[n // 2])
+    return {"median": med, "p10": pick(0.1), "p90": pick(0.9), "min": v[0], "max": v[-1],
+            "samples": n}
+
+
 def aggregate_rate(world, units_per_rank, seconds):
     """Whole-job rate under weak scaling: every rank processes the same units."""
     return world * units_per_rank / seconds
@@ -519,15 +532,23 @@ def ours_arm(args, rank, world, local_rank):
     sampler.mark_start()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # (eager) an event between consecutive steps gives each step's own device time
+    marks = ([torch.cuda.Event(enable_timing=True) for _ in range(args.steps - 1)]
+             if graph is None else [])
     e0.record(stream)
     if graph is not None:
         graph.replay()
     else:
-        for _ in range(args.steps):
+        for i in range(args.steps):
             step()
+            if i < args.steps - 1:
+                marks[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.mark_stop()
+    bounds = [e0, *marks, e1]
+    args.step_ms = (step_spread([a.elapsed_time(b) for a, b in zip(bounds, bounds[1:])])
+                    if graph is None else None)
     clocks = sampler.stop()
     barrier()
     prof = B.profile_read()
@@ -743,6 +764,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "step_ms": getattr(args, "step_ms", None),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": args.workload, "tokens": T, "d": d, "r": r,

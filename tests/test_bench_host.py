@@ -118,3 +118,11 @@ def test_dominant_kernel_skips_overlapped_operations():
     assert bench.dominant_kernel(prof, set())[0] == "gemm_wgrad_B"
     only = {"gemm_wgrad_B": (1, 1.0, 1.0, 1.0)}
     assert bench.dominant_kernel(only, set(bench.OVERLAPPED_OPS))[0] == "gemm_wgrad_B"
+
+
+def test_step_spread_median_and_percentiles():
+    s = bench.step_spread([5.0, 1.0, 3.0, 2.0, 4.0])
+    assert s == {"median": 3.0, "p10": 1.0, "p90": 5.0, "min": 1.0, "max": 5.0, "samples": 5}
+    s = bench.step_spread([float(i) for i in range(1, 11)])   # even count: mean of the middle two
+    assert s["median"] == 5.5 and s["p10"] == 2.0 and s["p90"] == 9.0 and s["samples"] == 10
+    assert bench.step_spread([]) is None
