@@ -677,6 +677,14 @@ cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void
   u.batch = static_cast<int32_t>(P.k);
   u.n_tiles = static_cast<int32_t>(cdiv(P.n, P.up.super_n()));
   u.m_inner = 0;
+  if (glu) {
+    // Grouped raster order, 8 rows of super-tiles at a time: with n fastest the gate, up
+    // and h tiles streaming through L2 evicted B between rows, and every row re-read all
+    // of B from DRAM. Measured on the 7B MLP at 8192 tokens: 290 -> 141 MB of DRAM
+    // reads, 260 -> 250 us; groups of 4 and 8 tie in the 16384-token step, 16 is slower.
+    static const int up_m_group = env_int("BOOST_UP_MGROUP", 8);
+    u.m_group = up_m_group;
+  }
   u.out = y;
   u.ldo = P.n;
   u.out_bstride = P.T * P.n;

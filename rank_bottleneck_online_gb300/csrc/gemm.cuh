@@ -100,6 +100,8 @@ struct GemmParams {
                               // a multiple of the launch's tile width)
   int32_t splits, kb_per_split;
   int32_t m_inner;            // tile order: 1 = m fastest within (batch, split)
+  int32_t m_group;            // m_inner == 0 and > 1: rows of super-tiles taken m fastest
+                              // in groups of this many, n next (grouped raster order)
   int32_t group_n;            // columns per group (grouped tiling)
   int32_t group_tiles;        // >0: N tiled per group, this many tiles per group
   int32_t act;                // 0 identity, 1 SiLU
@@ -201,6 +203,15 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int32_t ti
   if (p.m_inner) {
     mb = rem % p.m_tiles;
     nb = rem / p.m_tiles;
+  } else if (p.m_group > 1) {
+    // group g holds super-tile rows [g G, g G + gm) (gm < G in the last group), all n;
+    // within it m is fastest, so a wave shares B columns and the group's rows of A
+    const int32_t full = p.m_group * p.n_tiles;
+    const int32_t g = rem / full;
+    const int32_t gm = min(p.m_group, p.m_tiles - g * p.m_group);
+    const int32_t idx = rem - g * full;
+    mb = g * p.m_group + idx % gm;
+    nb = idx / gm;
   } else {
     nb = rem % p.n_tiles;
     mb = rem / p.n_tiles;
