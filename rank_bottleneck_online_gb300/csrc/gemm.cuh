@@ -453,21 +453,29 @@ struct EpiLoader {
   int32_t row_off, col_off;               // this warp's rows / this pair's columns in a tile
   int half;
   uint32_t issued, consumed;
+  // coordinates of tile `decoded` (decoding takes integer divisions: once per tile, not
+  // once per chunk)
+  int32_t decoded, pn0, pend, m0;
 
   // Issue the loads of the next chunk this warp will write (if any) into the next slot.
   __device__ __forceinline__ void issue_next(int lane) {
     while (tile < num_tiles) {
-      const TileCoord tc = decode_tile<TILE_N, TILE_M>(*p, tile);
-      const int32_t pn0 = tc.n0 + col_off;
+      if (tile != decoded) {
+        const TileCoord tc = decode_tile<TILE_N, TILE_M>(*p, tile);
+        decoded = tile;
+        pn0 = tc.n0 + col_off;
+        pend = min(pn0 + BN, tc.n_end);
+        m0 = tc.m0;
+      }
       const int32_t col0 = pn0 + (half + j * kEpiHalves) * 32;
-      if (j < kChunks && col0 < min(pn0 + BN, tc.n_end)) {
+      if (j < kChunks && col0 < pend) {
         const uint32_t slot = issued % kDepth;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars[slot], kSlotBytes);
 #pragma unroll
           for (int t = 0; t < kStreams; ++t)
             tma_load_3d(slots + slot * kSlotBytes + t * 2048, &p->tmE[t], &bars[slot], col0,
-                        tc.m0 + row_off, 0);
+                        m0 + row_off, 0);
         }
         ++issued;
         ++j;
@@ -618,9 +626,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float dgo[2], duo[2];
+          const uint32_t dh2 = pack_bf16x2(v[i], v[i + 1]);   // both rounded in one convert
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float dh = __bfloat162float(__float2bfloat16_rn(v[i + h]));
+            const float dh = h == 0 ? bf16_lo(dh2) : bf16_hi(dh2);
             const float z = gu[0][i + h];
             const float sg = sigmoid_f(z);
             dgo[h] = dh * gu[1][i + h] * (sg * (1.0f + z * (1.0f - sg)));
@@ -1032,6 +1041,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       ld.half = half;
       ld.issued = 0;
       ld.consumed = 0;
+      ld.decoded = -1;
     }
     ld.start(lane);
     int acc = 0;
