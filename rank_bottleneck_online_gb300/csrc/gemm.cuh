@@ -48,9 +48,18 @@ namespace boost_gb300 {
 constexpr int kBM = 128;           // rows per tile (TMEM lanes)
 constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;         // K per tcgen05.mma (kind::f16)
-constexpr int kEpiWarps = 8;       // two per TMEM lane quarter, alternating 32-column chunks
+// Epilogue warps: kEpiWarps (two per TMEM lane quarter, alternating 32-column chunks).
+// The SwiGLU-backward mode takes kGluEpiWarps (CTA pairs only); 12 (three per quarter,
+// 128 registers a thread) measured slower than 8 on the 7B MLP: the extra staging cost
+// the mainloop an operand stage (5 -> 4). Modes that write per-row partial sums (one row
+// per column tile and warp of a lane quarter) keep kEpiWarps, which the host sizes those
+// partials with.
+constexpr int kEpiWarps = 8;
 constexpr int kEpiHalves = kEpiWarps / 4;
-constexpr int kNumThreads = 32 * (2 + kEpiWarps);   // producer, MMA issuer, epilogue
+#ifndef BOOST_GLU_EPI_WARPS
+#define BOOST_GLU_EPI_WARPS 8
+#endif
+constexpr int kGluEpiWarps = BOOST_GLU_EPI_WARPS;
 
 enum EpiMode : int {
   EPI_ACT = 0,     // out_bf16 = act(s_row * acc)               (down-projection fwd)
@@ -125,6 +134,10 @@ struct GemmParams {
 
 template <int BN, int MODE, int CG, int MCM = 1, int MCN = 1>
 struct GemmCfg {
+  // (single-CTA tiles stage twice the B rows: no room for the extra warps' staging)
+  static constexpr int kEpiW = (MODE == EPI_GLU && CG == 2) ? kGluEpiWarps : kEpiWarps;
+  static constexpr int kHalves = kEpiW / 4;                     // warps per lane quarter
+  static constexpr int kThreads = 32 * (2 + kEpiW);             // producer, MMA, epilogue
   // two accumulators per tile, one per segment
   static constexpr bool kDual = (MODE == EPI_DUAL || MODE == EPI_UPGLU);
   static constexpr int kBRows = BN / CG;                          // B rows staged per CTA
@@ -150,8 +163,8 @@ struct GemmCfg {
   static constexpr int kLoadBytes =
       kEpiStreams > 0 ? kEpiDepth * kEpiStreams * 2048 : (MODE == EPI_DA ? 2048 : 0);
   static constexpr int kWarpStg = (MODE == EPI_F32) ? 4096 : kLoadBytes + 2048 * kStoreSlots;
-  static constexpr int kLdBars = kEpiStreams > 0 ? kEpiWarps * kEpiDepth : 0;
-  static constexpr int kStgBytes = kEpiWarps * kWarpStg;
+  static constexpr int kLdBars = kEpiStreams > 0 ? kEpiW * kEpiDepth : 0;
+  static constexpr int kStgBytes = kEpiW * kWarpStg;
   static constexpr int kStagesRaw = (232448 - 2048 - kStgBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kAccCols = kDual ? 2 * BN : BN;            // columns per accumulator set
@@ -184,6 +197,10 @@ struct GemmCfg {
   static_assert(kBRows % 64 == 0, "each CTA stages whole 64-row B boxes");
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit per CTA");
+  static_assert(kEpiW % 4 == 0 && kEpiW >= 4 && kEpiW <= 16, "whole lane quarters");
+  static_assert((MODE != EPI_DUAL && MODE != EPI_DA) || kHalves == kEpiHalves,
+                "per-row partial sums are sized for the default epilogue warps");
+  static_assert(MODE != EPI_UPGLU || (BN / 32) % kHalves == 0, "whole chunks per warp");
 };
 
 struct TileCoord {
@@ -441,9 +458,9 @@ __device__ __forceinline__ void slot_row_f32(const uint8_t* slot, int lane, floa
 // kDepth slots, kDepth chunks ahead of the consumer. The loads do not depend on the
 // accumulator, so the next tile's first chunks are in flight before its MMAs finish.
 // Lane 0 issues; every lane waits on the slot's mbarrier (bounded) before reading.
-template <int BN, int TILE_N, int TILE_M, int kStreams, int kDepth>
+template <int BN, int TILE_N, int TILE_M, int kStreams, int kDepth, int kHalves>
 struct EpiLoader {
-  static constexpr int kChunks = BN / 32 / kEpiHalves;
+  static constexpr int kChunks = (BN / 32 + kHalves - 1) / kHalves;   // most chunks a warp takes
   static constexpr int kSlotBytes = kStreams * 2048;
   const GemmParams* p;
   uint8_t* slots;          // kDepth slots of kStreams 2 KB blocks
@@ -467,7 +484,7 @@ struct EpiLoader {
         pend = min(pn0 + BN, tc.n_end);
         m0 = tc.m0;
       }
-      const int32_t col0 = pn0 + (half + j * kEpiHalves) * 32;
+      const int32_t col0 = pn0 + (half + j * kHalves) * 32;
       if (j < kChunks && col0 < pend) {
         const uint32_t slot = issued % kDepth;
         if (lane == 0) {
@@ -532,11 +549,12 @@ __device__ __forceinline__ void count_writes(const GemmParams& p, int64_t base, 
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
 // `col_tile` indexes the per-row partial sums (q, dgamma) of this BN-wide column tile.
-// `half` selects the 32-column chunks of this warp (half, half + kEpiHalves, ...); the
-// per-row partial sums are written per half, at row col_tile * kEpiHalves + half.
+// `half` selects the 32-column chunks of this warp (half, half + kHalves, ...), kHalves
+// being the warps per lane quarter; the per-row partial sums are written per warp of a
+// quarter, at row col_tile * kHalves + half.
 // `stg` is the warp's load slot (fp32 staging for EPI_F32), `ring` its store slots, `ld`
 // its input stream (EPI_GLU, EPI_DX).
-template <int BN, int MODE, int kSlots, bool kTma, class Loader>
+template <int BN, int MODE, int kHalves, int kSlots, bool kTma, class Loader>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc,
                                               int32_t row0, int32_t n0, int32_t n_end,
                                               uint32_t t_row, uint8_t* stg,
@@ -563,7 +581,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     if (p.gamma != nullptr && row_ok) g_row = __bfloat162float(p.gamma[row]);
   }
 #pragma unroll 1
-  for (int c = half; c < BN / 32; c += kEpiHalves) {
+  for (int c = half; c < BN / 32; c += kHalves) {
     const int32_t col0 = n0 + c * 32;
     const int cols_valid = n_end - col0;
     if (cols_valid <= 0) break;            // warp-uniform: the rest of the tile is outside N
@@ -674,11 +692,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
   if constexpr (MODE == EPI_DUAL) {
     if (row_ok && p.qpart != nullptr)
-      p.qpart[static_cast<int64_t>(col_tile * kEpiHalves + half) * p.M + row] = rowsum;
+      p.qpart[static_cast<int64_t>(col_tile * kHalves + half) * p.M + row] = rowsum;
   }
   if constexpr (MODE == EPI_DA) {
     if (row_ok && p.dgpart != nullptr)
-      p.dgpart[static_cast<int64_t>(col_tile * kEpiHalves + half) * p.M + row] = rowsum;
+      p.dgpart[static_cast<int64_t>(col_tile * kHalves + half) * p.M + row] = rowsum;
   }
 }
 
@@ -688,7 +706,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoid_f(g) * u; }
 
 // Epilogue of the fused up-projection + SwiGLU forward for the calling warp (rows
-// [row0, row0 + 32), columns [n0, n_end), the 32-column chunks half, half + kEpiHalves,
+// [row0, row0 + 32), columns [n0, n_end), the 32-column chunks half, half + kHalves,
 // ...). Accumulator 0 (gate, TMEM columns [0, BN)) is read first and kept in registers
 // as bf16; then, if `release0` is set, this warp's arrival on it lets the MMA warp start
 // the next tile's gate segment. Accumulator 1 (up, columns [BN, 2 BN)) is read next,
@@ -697,13 +715,13 @@ __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoid
 // h = silu(gate) * up stores. Gate and up of the warp's columns take 128 registers a
 // thread, so the TMEM loads are 16 columns wide to keep the transient small. The stores
 // go through the output maps only (the launch requires both).
-template <int BN, int CG, int kSlots, bool kTma>
+template <int BN, int CG, int kHalves, int kSlots, bool kTma>
 __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0, int32_t n0,
                                                int32_t n_end, uint32_t t_row,
                                                StoreRing<kSlots, kTma>& ring, int lane, int half,
                                                uint64_t* release0, uint64_t* release1,
                                                uint32_t leader_rank) {
-  constexpr int kChunks = BN / 32 / kEpiHalves;
+  constexpr int kChunks = BN / 32 / kHalves;
   const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
   __nv_bfloat16* y0 = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(row0) * p.ldo;
   __nv_bfloat16* y1 = y0 + p.out_bstride;
@@ -720,7 +738,7 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
   uint32_t uk[kChunks][16];
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) {
-    const int c = half + j * kEpiHalves;
+    const int c = half + j * kHalves;
     if (n0 + c * 32 < n_end) {              // warp-uniform
 #pragma unroll
       for (int hh16 = 0; hh16 < 2; ++hh16) {
@@ -735,7 +753,7 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
   if (release0 != nullptr) release(release0);
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) {
-    const int c = half + j * kEpiHalves;
+    const int c = half + j * kHalves;
     if (n0 + c * 32 < n_end) {              // warp-uniform
 #pragma unroll
       for (int hh16 = 0; hh16 < 2; ++hh16) {   // 16 columns per load: fewer live registers
@@ -750,7 +768,7 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
   release(release1);
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) {
-    const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
+    const int32_t col0 = n0 + (half + j * kHalves) * 32;
     if (col0 < n_end) {                     // warp-uniform
       store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], true, col0, row0, 0,
                        y0 + col0, p.ldo, rows_valid, n_end - col0);
@@ -770,7 +788,7 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
   if (p.visits != nullptr) {                // debug write counting (gate and up)
 #pragma unroll 1
     for (int j = 0; j < kChunks; ++j) {
-      const int32_t col0 = n0 + (half + j * kEpiHalves) * 32;
+      const int32_t col0 = n0 + (half + j * kHalves) * 32;
       if (col0 < n_end) {
         const int64_t base = static_cast<int64_t>(row0) * p.ldo + col0;
         count_writes(p, base, lane, rows_valid, n_end - col0);
@@ -781,7 +799,7 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
 }
 
 template <int BN, int MODE, int CG, int MCM, int MCN>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = GemmCfg<BN, MODE, CG, MCM, MCN>;
   constexpr int CL = Cfg::kCluster;
@@ -818,7 +836,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     for (int s = 0; s < Cfg::kAccStages; ++s) mbar_init(&tfull_bar[s], 1);
     for (int s = 0; s < Cfg::kTemptyBars; ++s)
-      mbar_init(&tempty_bar[s], kEpiWarps * CG);   // one arrival per epilogue warp of the pair
+      mbar_init(&tempty_bar[s], Cfg::kEpiW * CG);   // one arrival per epilogue warp of the pair
     mbar_init(done_bar, 1);
     for (int s = 0; s < Cfg::kLdBars; ++s) mbar_init(&ld_bar[s], 1);
     fence_barrier_init();
@@ -1026,7 +1044,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     constexpr int kStreams = Cfg::kEpiStreams > 0 ? Cfg::kEpiStreams : 1;
     using Loader = typename std::conditional<
         (Cfg::kEpiStreams > 0),
-        EpiLoader<BN, Cfg::kTileN, Cfg::kTileM, kStreams, Cfg::kEpiDepth>, NoLoader>::type;
+        EpiLoader<BN, Cfg::kTileN, Cfg::kTileM, kStreams, Cfg::kEpiDepth, Cfg::kHalves>,
+        NoLoader>::type;
     Loader ld{};
     if constexpr (Cfg::kEpiStreams > 0) {
       ld.p = &p;
@@ -1058,12 +1077,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int32_t pn0 = tc.n0 + static_cast<int32_t>(pn) * BN;
       const int32_t pend = min(pn0 + BN, tc.n_end);
       if constexpr (MODE == EPI_UPGLU) {
-        epilogue_upglu<BN, CG, Cfg::kStoreSlots, Cfg::kTmaStore>(
+        epilogue_upglu<BN, CG, Cfg::kHalves, Cfg::kStoreSlots, Cfg::kTmaStore>(
             p, row0, pn0, pend, t_row, ring, lane, half,
             Cfg::kSplitRelease ? &tempty_bar[0] : nullptr,
             &tempty_bar[Cfg::kSplitRelease ? 1 : acc], leader_rank);
       } else {
-        epilogue_tile<BN, MODE, Cfg::kStoreSlots, Cfg::kTmaStore>(
+        epilogue_tile<BN, MODE, Cfg::kHalves, Cfg::kStoreSlots, Cfg::kTmaStore>(
             p, tc, row0, pn0, pend, t_row, stg, ring, ld, lane,
             tc.n_blk * MCN + static_cast<int32_t>(pn), half);
       }
