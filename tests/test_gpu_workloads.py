@@ -66,13 +66,15 @@ def test_fused_swiglu_backward_matches_separate_passes(T, d, r, ffn):
 
 
 @pytest.mark.parametrize("T,d,r,n", [(512, 256, 128, 512), (600, 128, 64, 520), (300, 128, 64, 200),
-                                     (4352, 256, 128, 1024)])
+                                     (4352, 256, 128, 1024), (6000, 256, 128, 1040)])
 def test_fused_swiglu_forward_matches_separate_passes(T, d, r, n):
     # the gate/up up-projection with two accumulators and SwiGLU in its epilogue gives
     # the batched up-projection's gate and up bit for bit, and the stand-alone SwiGLU
     # pass's h bit for bit (same MMAs, same K order, same expression). Shapes: 2 x 2
-    # clusters with one accumulator set (early release of the gate accumulator), a
-    # ragged last column tile, 128-wide double-buffered tiles, co-scheduled rows.
+    # clusters with one accumulator set (early release of both accumulators), a ragged
+    # last column tile, 128-wide double-buffered tiles, co-scheduled rows; at 6000
+    # tokens the cluster launch's rows of super-tiles form one full group of the
+    # grouped raster order and a shorter last group.
     w = inputs.make_block(T, d, r, 2, n, seed=7)
     blk = Block(T, d, r, 2, n, S=4, weights=w)
     x = w["x"].cuda()
