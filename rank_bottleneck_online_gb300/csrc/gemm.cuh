@@ -73,7 +73,13 @@ enum EpiMode : int {
                    // out2 = h = bf16(silu(gate) * up)     (up-projection + SwiGLU fwd)
   EPI_BF16T = 8,   // EPI_BF16 through TMA stores (short-K up-projections, where the
                    // epilogue's stores weigh most)
+  EPI_DUALT = 9,   // EPI_DUAL through TMA stores (short K: the epilogue weighs more)
 };
+
+// the two dual-accumulator recompute + dgrad modes
+__host__ __device__ constexpr bool is_dual(int mode) {
+  return mode == EPI_DUAL || mode == EPI_DUALT;
+}
 
 struct OperandView {
   int8_t mn_dim;    // tensor-map dimension carrying the M (or N) index
@@ -139,7 +145,7 @@ struct GemmCfg {
   static constexpr int kHalves = kEpiW / 4;                     // warps per lane quarter
   static constexpr int kThreads = 32 * (2 + kEpiW);             // producer, MMA, epilogue
   // two accumulators per tile, one per segment
-  static constexpr bool kDual = (MODE == EPI_DUAL || MODE == EPI_UPGLU);
+  static constexpr bool kDual = (is_dual(MODE) || MODE == EPI_UPGLU);
   static constexpr int kBRows = BN / CG;                          // B rows staged per CTA
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = kBRows * kBK * 2;
@@ -149,7 +155,8 @@ struct GemmCfg {
   // pays where the epilogue is the bottleneck (the SwiGLU epilogues); elsewhere they
   // compete with the operand loads for the SM's TMA unit, and plain coalesced stores
   // through the warp's staging block measured faster.
-  static constexpr bool kTmaStore = (MODE == EPI_GLU || MODE == EPI_UPGLU || MODE == EPI_BF16T);
+  static constexpr bool kTmaStore =
+      (MODE == EPI_GLU || MODE == EPI_UPGLU || MODE == EPI_BF16T || MODE == EPI_DUALT);
   // Epilogue inputs streamed by TMA (EpiLoader): gate and up for EPI_GLU, x for EPI_DX,
   // kEpiDepth chunks ahead of the consumer. One chunk ahead measured faster than two:
   // the shared memory a second slot takes costs the mainloop a pipeline stage, and these
@@ -198,7 +205,7 @@ struct GemmCfg {
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit per CTA");
   static_assert(kEpiW % 4 == 0 && kEpiW >= 4 && kEpiW <= 16, "whole lane quarters");
-  static_assert((MODE != EPI_DUAL && MODE != EPI_DA) || kHalves == kEpiHalves,
+  static_assert((!is_dual(MODE) && MODE != EPI_DA) || kHalves == kEpiHalves,
                 "per-row partial sums are sized for the default epilogue warps");
   static_assert(MODE != EPI_UPGLU || (BN / 32) % kHalves == 0, "whole chunks per warp");
 };
@@ -564,7 +571,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   const bool row_ok = row < p.M;
   const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
   float s_row = 1.0f;
-  if constexpr (MODE == EPI_ACT || MODE == EPI_DUAL || MODE == EPI_DX) {
+  if constexpr (MODE == EPI_ACT || is_dual(MODE) || MODE == EPI_DX) {
     if (p.rstd != nullptr && row_ok) s_row = p.rstd[row];
   }
   float rowsum = 0.0f;
@@ -589,7 +596,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     float v[32];
     tmem_ld_32x32b_x32(t_row + c * 32, v);
     float w[32];
-    if constexpr (MODE == EPI_DUAL) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
+    if constexpr (is_dual(MODE)) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
     tmem_ld_wait();
     if constexpr (MODE == EPI_F32) {
       const int64_t base = tc.split * p.out_sstride + tc.batch * p.out_bstride +
@@ -607,7 +614,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       } else if constexpr (MODE == EPI_BF16 || MODE == EPI_BF16T) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-      } else if constexpr (MODE == EPI_DUAL) {
+      } else if constexpr (is_dual(MODE)) {
         // a = act(z) (recompute) and dzs = s * act'(z) * (dy B^T); row partial of dz * z.
         uint32_t pk2[16];
 #pragma unroll
@@ -690,7 +697,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
     }
   }
-  if constexpr (MODE == EPI_DUAL) {
+  if constexpr (is_dual(MODE)) {
     if (row_ok && p.qpart != nullptr)
       p.qpart[static_cast<int64_t>(col_tile * kHalves + half) * p.M + row] = rowsum;
   }
