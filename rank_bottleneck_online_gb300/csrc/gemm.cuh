@@ -409,7 +409,7 @@ struct StoreRing {
 // which clips rows and columns outside the map; the warp does not wait for the global
 // write. With `tma` false (no map, or the chunk is cut by a group boundary inside the
 // tensor, which the map cannot clip) it is written with coalesced plain stores instead.
-template <int kSlots, bool kTma>
+template <int kSlots, bool kTma, bool kEvictFirst = false>
 __device__ __forceinline__ void store_chunk_bf16(StoreRing<kSlots, kTma>& ring, int lane,
                                                  const uint32_t (&pk)[16], const CUtensorMap* tm,
                                                  bool tma, int32_t col0, int32_t row0,
@@ -435,7 +435,8 @@ __device__ __forceinline__ void store_chunk_bf16(StoreRing<kSlots, kTma>& ring, 
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_3d(tm, slot, col0, row0, batch);
+      if constexpr (kEvictFirst) tma_store_3d_hint(tm, slot, col0, row0, batch, l2_evict_first());
+      else tma_store_3d(tm, slot, col0, row0, batch);
       bulk_commit_group();
     }
   } else {
@@ -468,6 +469,8 @@ __device__ __forceinline__ void slot_row_f32(const uint8_t* slot, int lane, floa
 template <int BN, int TILE_N, int TILE_M, int kStreams, int kDepth, int kHalves>
 struct EpiLoader {
   static constexpr int kChunks = (BN / 32 + kHalves - 1) / kHalves;   // most chunks a warp takes
+  // gate and up of the SwiGLU backward are read once: keep them from displacing operands
+  static constexpr bool kEvictFirst = (kStreams == 2);
   static constexpr int kSlotBytes = kStreams * 2048;
   const GemmParams* p;
   uint8_t* slots;          // kDepth slots of kStreams 2 KB blocks
@@ -498,8 +501,12 @@ struct EpiLoader {
           mbar_arrive_expect_tx(&bars[slot], kSlotBytes);
 #pragma unroll
           for (int t = 0; t < kStreams; ++t)
-            tma_load_3d(slots + slot * kSlotBytes + t * 2048, &p->tmE[t], &bars[slot], col0,
-                        m0 + row_off, 0);
+            if constexpr (kEvictFirst)
+              tma_load_3d_hint(slots + slot * kSlotBytes + t * 2048, &p->tmE[t], &bars[slot],
+                               col0, m0 + row_off, 0, l2_evict_first());
+            else
+              tma_load_3d(slots + slot * kSlotBytes + t * 2048, &p->tmE[t], &bars[slot], col0,
+                          m0 + row_off, 0);
         }
         ++issued;
         ++j;
@@ -665,8 +672,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         }
         __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
                             static_cast<int64_t>(row0) * p.ldo + col0;
-        store_chunk_bf16(ring, lane, pk2, &p.tmO[1], whole && (p.tma_out & 2), col0, row0, 0, o2,
-                         p.ldo, rows_valid, cols_valid);
+        // (dgate and dup are written once here: evict-first in L2)
+        store_chunk_bf16<kSlots, kTma, true>(ring, lane, pk2, &p.tmO[1],
+                                             whole && (p.tma_out & 2), col0, row0, 0, o2,
+                                             p.ldo, rows_valid, cols_valid);
       } else if constexpr (MODE == EPI_DX) {
         float xv[1][32];
         if (p.tma_in) {                          // RMSNorm term: x streamed by the loader
@@ -692,8 +701,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
           pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
       }
       const int64_t base = tc.batch * p.out_bstride + static_cast<int64_t>(row0) * p.ldo + col0;
-      store_chunk_bf16(ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
-                       static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
+      store_chunk_bf16<kSlots, kTma, MODE == EPI_GLU>(
+          ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
+          static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
       if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
     }
   }
@@ -721,7 +731,7 @@ __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoid
 // store: the next tile's MMAs then overlap all of this tile's gate, up and
 // h = silu(gate) * up stores. Gate and up of the warp's columns take 128 registers a
 // thread, so the TMEM loads are 16 columns wide to keep the transient small. The stores
-// go through the output maps only (the launch requires both).
+// go through the output maps only (the launch requires both), evict-first in L2.
 template <int BN, int CG, int kHalves, int kSlots, bool kTma>
 __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0, int32_t n0,
                                                int32_t n_end, uint32_t t_row,
@@ -777,10 +787,10 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
   for (int j = 0; j < kChunks; ++j) {
     const int32_t col0 = n0 + (half + j * kHalves) * 32;
     if (col0 < n_end) {                     // warp-uniform
-      store_chunk_bf16(ring, lane, gk[j], &p.tmO[0], true, col0, row0, 0,
-                       y0 + col0, p.ldo, rows_valid, n_end - col0);
-      store_chunk_bf16(ring, lane, uk[j], &p.tmO[0], true, col0, row0, 1,
-                       y1 + col0, p.ldo, rows_valid, n_end - col0);
+      store_chunk_bf16<kSlots, kTma, true>(ring, lane, gk[j], &p.tmO[0], true, col0, row0, 0,
+                                           y0 + col0, p.ldo, rows_valid, n_end - col0);
+      store_chunk_bf16<kSlots, kTma, true>(ring, lane, uk[j], &p.tmO[0], true, col0, row0, 1,
+                                           y1 + col0, p.ldo, rows_valid, n_end - col0);
       // h after gate and up have gone to shared memory, in place of this chunk's gate
       // registers (the live set stays at gate + up)
 #pragma unroll
@@ -788,8 +798,8 @@ __device__ __forceinline__ void epilogue_upglu(const GemmParams& p, int32_t row0
         gk[j][i] = pack_bf16x2(swiglu_h(bf16_lo(gk[j][i]), bf16_lo(uk[j][i])),
                                swiglu_h(bf16_hi(gk[j][i]), bf16_hi(uk[j][i])));
       const uint32_t (&hk)[16] = gk[j];
-      store_chunk_bf16(ring, lane, hk, &p.tmO[1], true, col0, row0, 0,
-                       hh + col0, p.ldo, rows_valid, n_end - col0);
+      store_chunk_bf16<kSlots, kTma, true>(ring, lane, hk, &p.tmO[1], true, col0, row0, 0,
+                                           hh + col0, p.ldo, rows_valid, n_end - col0);
     }
   }
   if (p.visits != nullptr) {                // debug write counting (gate and up)
