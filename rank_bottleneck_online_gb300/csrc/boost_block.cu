@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -59,21 +60,23 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // --------------------------------------------------------------- devices
 int current_num_sms() {
-  static int cache[64] = {0};
+  // per-device cache; host threads may fill it concurrently (same value)
+  static std::atomic<int> cache[64];
+  constexpr int kFallback = 152;   // GB300; only when the runtime cannot be asked
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
-    return 148;
+    return kFallback;
   }
-  if (cache[dev] == 0) {
+  if (cache[dev].load(std::memory_order_relaxed) == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
       cudaGetLastError();
-      return 148;
+      return kFallback;
     }
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return cache[dev].load(std::memory_order_relaxed);
 }
 
 uint64_t wait_limit_ns() {
