@@ -25,10 +25,11 @@
 // pair of the cluster has released it.
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the
 // mainloop of tile i+1, except with two 256-column accumulators per tile (EPI_DUAL,
-// EPI_UPGLU), which fill TMEM; EPI_UPGLU then frees each accumulator as soon as it
-// has been read into registers, before its stores. A launch may cover a row range (m_base, m_extent) or start at a
-// column (n_base) of the output, so that two launches of different cluster shapes can
-// share one GEMM. Every mbarrier wait is bounded (ptx.cuh).
+// EPI_DUALT, EPI_UPGLU), which fill TMEM; EPI_UPGLU then frees each accumulator as
+// soon as it has been read into registers, before its stores. A launch may cover a
+// row range (m_base, m_extent) or start at a column (n_base) of the output, so that
+// two launches of different cluster shapes can share one GEMM. Every mbarrier wait is
+// bounded (ptx.cuh).
 //
 // Operands are described by "views" of 3-D tensor maps: which map dimension
 // carries the MN index, which the K index and which the batch index, and whether
@@ -526,7 +527,8 @@ struct EpiLoader {
     const uint32_t slot = consumed % kDepth;
     bounded_wait(&bars[slot], (consumed / kDepth) & 1u, p->err, 9, p->wait_limit_ns);
 #pragma unroll
-    for (int t = 0; t < kStreams; ++t) slot_row_f32(slots + slot * kSlotBytes + t * 2048, lane, out[t]);
+    for (int t = 0; t < kStreams; ++t)
+      slot_row_f32(slots + slot * kSlotBytes + t * 2048, lane, out[t]);
     ++consumed;
     fence_proxy_async_smem();   // these reads precede the next TMA write into the slot
     __syncwarp();
@@ -894,7 +896,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
         const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
         const int32_t m_own =
             tc.m0 + static_cast<int32_t>(pm) * (kBM * CG) + static_cast<int32_t>(rank) * kBM;
-        const int32_t n_half = static_cast<int32_t>(pn) * BN + static_cast<int32_t>(rank) * Cfg::kBRows;
+        const int32_t n_half =
+            static_cast<int32_t>(pn) * BN + static_cast<int32_t>(rank) * Cfg::kBRows;
         for (int sg = 0; sg < p.num_seg && ok; ++sg) {
           const Segment& S = p.seg[sg];
           int32_t b = tc.batch;
@@ -1072,7 +1075,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
       ld.tile_stride = tile_stride;
       ld.num_tiles = p.tma_in ? num_tiles : 0;
       ld.j = 0;
-      ld.row_off = static_cast<int32_t>(pm) * (kBM * CG) + static_cast<int32_t>(rank) * kBM + q * 32;
+      ld.row_off =
+          static_cast<int32_t>(pm) * (kBM * CG) + static_cast<int32_t>(rank) * kBM + q * 32;
       ld.col_off = static_cast<int32_t>(pn) * BN;
       ld.half = half;
       ld.issued = 0;

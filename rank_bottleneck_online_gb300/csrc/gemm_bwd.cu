@@ -7,8 +7,8 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p, int num_sms,
-                                  cudaStream_t stream) {
+cudaError_t launch_gemm_bwd_modes(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p,
+                                  int num_sms, cudaStream_t stream) {
   if (mode == EPI_DUAL) return launch_mode<EPI_DUAL>(bn, cg, mcm, mcn, p, num_sms, stream);
   if (mode == EPI_DUALT) return launch_mode<EPI_DUALT>(bn, cg, mcm, mcn, p, num_sms, stream);
   if (mode == EPI_DX) return launch_mode<EPI_DX>(bn, cg, mcm, mcn, p, num_sms, stream);

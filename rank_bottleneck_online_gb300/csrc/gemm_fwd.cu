@@ -7,8 +7,8 @@
 
 namespace boost_gb300 {
 
-cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p, int num_sms,
-                                  cudaStream_t stream) {
+cudaError_t launch_gemm_fwd_modes(int bn, int mode, int cg, int mcm, int mcn, const GemmParams& p,
+                                  int num_sms, cudaStream_t stream) {
   if (mode == EPI_ACT) return launch_mode<EPI_ACT>(bn, cg, mcm, mcn, p, num_sms, stream);
   if (mode == EPI_BF16) return launch_mode<EPI_BF16>(bn, cg, mcm, mcn, p, num_sms, stream);
   if (mode == EPI_UPGLU) return launch_mode<EPI_UPGLU>(bn, cg, mcm, mcn, p, num_sms, stream);

@@ -76,8 +76,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed, for at most
 // limit_ns nanoseconds. On expiry (or when another role already gave up) the
 // error word is set and false is returned; the caller then stops its loop.
-static __device__ __noinline__ bool bounded_wait_slow(uint64_t* bar, uint32_t parity, DeviceError* err,
-                                               uint32_t where, uint64_t limit_ns) {
+static __device__ __noinline__ bool bounded_wait_slow(uint64_t* bar, uint32_t parity,
+                                                      DeviceError* err, uint32_t where,
+                                                      uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -327,7 +328,8 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
 __device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* tmap, uint32_t bar,
                                                  int32_t c0, int32_t c1, int32_t c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
@@ -389,7 +391,8 @@ __device__ __forceinline__ void tma_load_3d_pair_mc(void* dst, const void* tmap,
                                                     uint16_t mask, int32_t c0, int32_t c1,
                                                     int32_t c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes"
       ".multicast::cluster [%0], [%1, {%4, %5, %6}], [%2], %3;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "h"(mask), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
