@@ -126,3 +126,41 @@ def test_step_spread_median_and_percentiles():
     s = bench.step_spread([float(i) for i in range(1, 11)])   # even count: mean of the middle two
     assert s["median"] == 5.5 and s["p10"] == 2.0 and s["p90"] == 9.0 and s["samples"] == 10
     assert bench.step_spread([]) is None
+
+
+def test_report_line_carries_the_contract_keys(capsys):
+    # one JSON line with the keys the driver reads, from a synthetic profile (no GPU)
+    import argparse
+    import json
+
+    T, d, r, ffn, S, steps = 16384, 4096, 1024, 11008, 8, 10
+    args = argparse.Namespace(steps=steps, warmup=5, workload=bench.WORKLOAD, skip_aux=True,
+                              timing="eager",
+                              step_ms=bench.step_spread([3.7] * steps))
+    exe, _ = bench.workload_flops(bench.WORKLOAD, T)
+    ms_total = 37.0
+    # name -> (launches, ms, flops, bytes) over the timed steps
+    prof = {"gemm_dual": (2 * steps, 10.0, 0.3 * exe * steps, 1e9),
+            "gemm_up_swiglu": (steps, 5.0, 0.14 * exe * steps, 1e9),
+            "gemm_dx_swiglu": (steps, 4.0, 0.07 * exe * steps, 1e10),
+            "rmsnorm_stats": (steps, 0.3, 0.0, 1.3e9)}
+    clocks = {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert bench._report(args, 1, prof, {"gemm_dual": 4 * steps}, clocks, ms_total,
+                         float("nan"), 0, 0, T, d, r, ffn, S) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches", "step_ms"):
+        assert key in line, key
+    assert line["metric"] == bench.METRIC and line["unit"] == "tokens/s"
+    assert line["value"] == pytest.approx(T * steps / (ms_total / 1e3))
+    assert line["ms_per_step"] == pytest.approx(ms_total / steps)
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["n_gpus"] == 1 and line["config"]["workload"] == bench.WORKLOAD
+    roof = line["roofline"]
+    assert {"bound", "achieved", "peak", "unit", "frac", "traffic"} <= set(roof)
+    # the dominant kernel is taken among the operations timed alone (gemm_dual here)
+    assert roof["kernel"] == "gemm_dual" and roof["bound"] == "tensor"
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    assert line["gpu_launches"] == 4 * steps + 3 * steps   # kernels, not operations
+    assert line["step_ms"]["median"] == pytest.approx(3.7)
