@@ -11,8 +11,10 @@ gate/up activations 721 MB and their gradients) is larger than the 129 MB L2,
 so no L2 flush is inserted between steps.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-Multi-GPU (torchrun, one process per GPU) runs independent replicas (weak
-scaling); the only collectives are the timing barrier and the max over ranks.
+One GPU only: the GEMMs load their operands with cluster-multicast TMA copies, which
+may run only in single-GPU processes, so `--gpus N` with N > 1 (or a torchrun launch
+with WORLD_SIZE > 1) prints an `unavailable` line and exits 0 without launching a
+kernel. The reference arm (the CPU oracle) runs on rank 0 at any N.
 """
 
 from __future__ import annotations
@@ -188,25 +190,128 @@ def _cfg(name=WORKLOAD):
 
 # ------------------------------------------------------------- clocks
 
-class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples taken while the timed region runs.
+# NVML clock-event reason bits (nvmlClocksEventReason* in nvml.h) that the timing rules
+# name; the others (idle, application clocks, sync boost, ...) are not reported.
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown"}
 
-    nvidia-smi is started before the region (it takes a moment to deliver its first
-    sample) and every sample carries its timestamp; only samples taken between
-    mark_start() and mark_stop() are reported."""
+
+def summarize_clocks(samples, source, in_region=True):
+    """Summary of clock samples (sm_mhz, sm_max_mhz, power_w, set of reason names) taken
+    during the timed region: median SM clock, maximum clock and power, every reason seen,
+    and the share of samples with the power cap active."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "power_w_max": None, "reasons": [],
+                "samples": 0, "power_cap_share": None, "source": source}
+    sm = sorted(s[0] for s in samples)
+    n = len(sm)
+    med = sm[n // 2] if n % 2 else 0.5 * (sm[n // 2 - 1] + sm[n // 2])
+    seen = set()
+    for s in samples:
+        seen |= set(s[3])
+    out = {"sm_mhz": med, "sm_max_mhz": max(s[1] for s in samples),
+           "power_w_max": max(s[2] for s in samples), "reasons": sorted(seen),
+           "samples": n if in_region else 0,
+           "power_cap_share": sum(1 for s in samples if "sw_power_cap" in s[3]) / n,
+           "source": source}
+    if not in_region:
+        out["note"] = "no sample fell inside the timed region; nearest sample reported"
+    return out
+
+
+class _Nvml:
+    """The few read-only NVML queries the sampler needs, through ctypes on the driver's
+    libnvidia-ml (no Python NVML package on the GPU host)."""
+
+    def __init__(self, cuda_index):
+        import ctypes
+
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:                                   # the CUDA device's own GPU, by UUID
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            key = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid).encode()
+            ok = self.lib.nvmlDeviceGetHandleByUUID(key, ctypes.byref(self.h)) == 0
+        except Exception:  # noqa: BLE001
+            ok = False
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(
+                ctypes.c_uint(cuda_index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.sm_max = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, 1)
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        if fn(self.h, *args, self.c.byref(v)) != 0:
+            return None
+        return float(v.value)
+
+    def sample(self):
+        sm = self._uint(self.lib.nvmlDeviceGetClockInfo, 1)          # NVML_CLOCK_SM
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        bits = self.c.c_ulonglong()
+        names = set()
+        if self.reasons_fn(self.h, self.c.byref(bits)) == 0:
+            names = {nm for b, nm in NVML_REASONS.items() if bits.value & b}
+        if sm is None:
+            return None
+        return (sm, self.sm_max or sm, (mw or 0.0) / 1e3, names)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """SM clock, power and clock-event reasons sampled while the timed region runs.
+
+    Reads NVML every few milliseconds from a background thread (read-only queries);
+    where NVML cannot be loaded, nvidia-smi's own loop (100 ms) stands in. Every sample
+    carries its time, and only samples taken between mark_start() and mark_stop() are
+    reported (the nearest one, marked as such, if none fell inside)."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_S = 0.005
 
     def __init__(self, index):
-        self.index = str(index)
+        self.index = index
+        self.nvml = None
+        self.thread = None
+        self.samples = []          # (time, (sm, sm_max, power, reasons))
+        self.stopping = False
         self.proc = None
         self.out = None
         self.t0 = self.t1 = None
 
     def start(self):
+        try:
+            self.nvml = _Nvml(self.index)
+        except Exception:  # noqa: BLE001
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+
+            def loop():
+                while not self.stopping:
+                    try:
+                        s = self.nvml.sample()
+                    except Exception:  # noqa: BLE001  (a failed read is a missing sample)
+                        s = None
+                    if s is not None:
+                        self.samples.append((time.time(), s))
+                    time.sleep(self.PERIOD_S)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return
         try:
             self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
@@ -231,40 +336,66 @@ class ClockSampler:
         except ValueError:
             return None
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _smi_rows(self):
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.seek(0)
-        rows = [[c.strip() for c in l.split(",")] for l in self.out.read().splitlines()
-                if l.strip()]
+        rows = [[c.strip() for c in ln.split(",")] for ln in self.out.read().splitlines()
+                if ln.strip()]
         rows = [r for r in rows if len(r) >= 10]
-        if any(r[1] == self.index for r in rows):
-            rows = [r for r in rows if r[1] == self.index]
-        if self.t0 is not None and self.t1 is not None:
-            timed = [r for r in rows
-                     if (w := self._when(r[0])) is not None and self.t0 <= w <= self.t1]
-            rows = timed if timed else rows[-1:]
-        sm, smax, power, seen = [], [], [], set()
+        if any(r[1] == str(self.index) for r in rows):
+            rows = [r for r in rows if r[1] == str(self.index)]
+        out = []
         for r in rows:
             try:
-                sm.append(float(r[2]))
-                smax.append(float(r[3]))
-                power.append(float(r[4]))
+                s = (float(r[2]), float(r[3]), float(r[4]),
+                     {nm for nm, v in zip(self.NAMES, r[6:10]) if v.lower() == "active"})
             except ValueError:
                 continue
-            for nm, v in zip(self.NAMES, r[6:10]):
-                if v.lower() == "active":
-                    seen.add(nm)
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "reasons": sorted(seen), "samples": len(sm)}
+            w = self._when(r[0])
+            if w is not None:
+                out.append((w, s))
+        return out
+
+    def stop(self):
+        if self.nvml is not None:
+            self.stopping = True
+            self.thread.join(timeout=5)
+            self.nvml.close()
+            timed, source = list(self.samples), "nvml"
+        elif self.proc is not None:
+            timed, source = self._smi_rows(), "nvidia-smi"
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks unavailable"],
+                    "samples": 0, "power_cap_share": None, "source": None}
+        return self.select(timed, self.t0, self.t1, source)
+
+    @staticmethod
+    def select(timed, t0, t1, source):
+        """Summary of the (time, sample) pairs inside [t0, t1], else of the nearest one."""
+        inside = [s for w, s in timed if t0 is not None and t1 is not None and t0 <= w <= t1]
+        if inside or not timed:
+            return summarize_clocks(inside, source)
+        mid = 0.5 * (t0 + t1) if t0 is not None and t1 is not None else timed[-1][0]
+        near = min(timed, key=lambda ws: abs(ws[0] - mid))[1]
+        return summarize_clocks([near], source, in_region=False)
+
+
+def choose_peak(peaks, clocks):
+    """(kind, TFLOP/s) of the bf16 peak the dominant GEMM is set against.
+
+    The burst peak is a dense GEMM timed alone at full clock; the sustained one the same
+    GEMM held for seconds, where the 1.4 kW power cap pulls the SM clock down. A timed
+    region whose clock samples show the power cap in at least half of them ran under the
+    same conditions as the sustained measurement and takes that peak; any other region
+    (also one with no sample) takes the burst peak, the stricter denominator."""
+    share = (clocks or {}).get("power_cap_share")
+    if share is not None and share >= 0.5:
+        return "sustained", peaks["bf16_tflops_sustained"]
+    return "burst", peaks["bf16_tflops"]
 
 
 # ------------------------------------------------------------- oracle
@@ -458,7 +589,8 @@ def _workload_step(name, wl, w, dev):
     return lambda: (wl.forward(x), wl.backward(x, dq, dg))
 
 
-def ours_arm(args, rank, world, local_rank):
+def ours_arm(args):
+    """The library's timed step on this process's one GPU (cuda:0)."""
     import torch
 
     from rank_bottleneck_online_gb300 import binding as B
@@ -467,8 +599,8 @@ def ours_arm(args, rank, world, local_rank):
     from rank_bottleneck_online_gb300.block import MLP, build_workload
 
     build_mod.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     name = args.workload
     c = inputs.CONFIGS[name]
     T = args.tokens or c["T"]
@@ -494,15 +626,7 @@ def ours_arm(args, rank, world, local_rank):
         for ws in workspaces:
             B.check(ws)
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(0)
     sampler.start()                 # running before the timed region; samples filtered
     for _ in range(args.warmup):
         step()
@@ -527,7 +651,6 @@ def ours_arm(args, rank, world, local_rank):
             graph = None
             B.profile_enable(False)        # drop what the failed capture recorded
             B.profile_enable(True)
-    barrier()
     torch.cuda.synchronize()
     sampler.mark_start()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -550,31 +673,26 @@ def ours_arm(args, rank, world, local_rank):
     args.step_ms = (step_spread([a.elapsed_time(b) for a, b in zip(bounds, bounds[1:])])
                     if graph is None else None)
     clocks = sampler.stop()
-    barrier()
     prof = B.profile_read()
     prof_kernels = B.profile_kernels()
     B.profile_enable(False)
     args.timing = "cuda_graph" if graph is not None else "eager"
     del graph
     check()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    ms_total = e0.elapsed_time(e1)
     if mlp is None:             # the other workloads: the timed step and its roofline only
-        if rank != 0:
-            return 0
-        return _report(args, world, prof, prof_kernels, clocks, ms_total, float("nan"), 0, 0,
+        return _report(args, 1, prof, prof_kernels, clocks, ms_total, float("nan"), 0, 0,
                        T, c["d"], c["r"], c.get("ffn"), c["S"])
 
     aux = not args.skip_aux
-    e2e_s = _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev) if aux else float("nan")
-    btp = _btp_exchange(mlp, x, T, d, r, ffn, S) if aux and rank == 0 else None
-    dense = _dense_context(T, d, ffn, ms_total / args.steps) if aux and rank == 0 else None
+    e2e_s = _e2e(args, mlp, w, x, dout, T, d, dev) if aux else float("nan")
+    btp = _btp_exchange(mlp, x, T, d, r, ffn, S) if aux else None
+    dense = _dense_context(T, d, ffn, ms_total / args.steps) if aux else None
     cuts = (_checkpoint_cuts(mlp, w, x, dout, T, d, r, ffn, S, ms_total / args.steps)
-            if aux and rank == 0 else None)
+            if aux else None)
     bi = 2 * T * d * 2          # x and dout, bf16
     bo = 2 * T * d * 2          # out and dx, bf16
-    if rank != 0:
-        return 0
-    return _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r,
+    return _report(args, 1, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r,
                    ffn, S, btp, dense, cuts)
 
 
@@ -629,7 +747,7 @@ def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
                        "all-reduce of each low-rank pair's d-wide output ([T, k*n])"}
 
 
-def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
+def _e2e(args, mlp, w, x, dout, T, d, dev):
     """Seconds for args.steps steps through the public API from pinned host buffers:
     each step copies its x and dout in, runs forward + backward and copies out and dx
     back. The copies are pipelined against the compute on two more streams (inputs of
@@ -679,11 +797,10 @@ def _e2e(args, mlp, w, x, dout, T, d, barrier, dist, dev):
 
     run(2)
     torch.cuda.synchronize()
-    barrier()
     t0 = time.perf_counter()
     run(args.steps)
     torch.cuda.synchronize()
-    return max_over_ranks(time.perf_counter() - t0, dist, dev)
+    return time.perf_counter() - t0
 
 
 # Operations the library runs concurrently with other GEMMs (unless BOOST_FORK_STREAMS=0):
@@ -720,12 +837,14 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     bound = "tensor" if kfl > 0 else "hbm"
     if bound == "tensor":
         achieved = kfl / (kms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak_kind, peak = choose_peak(peaks, clocks)
+        fracs = {"frac_burst": achieved / peaks["bf16_tflops"],
+                 "frac_sustained": achieved / peaks["bf16_tflops_sustained"]}
         unit = "TFLOP/s"
         per_launch_units = kfl / launches
     else:
         achieved = kby / (kms / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
+        peak_kind, peak, fracs = "copy", peaks["hbm_gbs"], {}
         unit = "GB/s"
         per_launch_units = kby / launches
     # (the committed counters are for the default workload's shapes)
@@ -770,7 +889,7 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
         "config": {"workload": args.workload, "tokens": T, "d": d, "r": r,
                    **({"ffn": ffn} if ffn else {}), "S": S,
                    **({k: v for k, v in _cfg(args.workload).items() if k in ("k", "n", "kind")}),
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "parallelism": "single",
                    "l2": "inputs larger than L2 (no flush)",
                    "launch": getattr(args, "timing", "eager")},
         "tflops_per_s": tflops,
@@ -781,10 +900,12 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
                           "peak_tflops": peaks["bf16_tflops"], "peak_gbs": peaks["hbm_gbs"],
                           "peaks": f"{peaks['source']} burst"},
         "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                     "unit": unit, "frac": achieved / peak, **fracs, "traffic": traffic,
                      "launches_per_step": launches / args.steps,
-                     "peak_kind": (f"{peaks['source']} sustained" if bound == "tensor"
-                                   else peaks["source"])},
+                     "peak_kind": f"{peaks['source']} {peak_kind}",
+                     "peak_choice": ("sustained when the power cap is active in at least "
+                                     "half of the timed region's clock samples, else burst")
+                     if bound == "tensor" else None},
         "kernels": kernels,
         "gpu_launches": gpu_launches,
         "e2e": None if args.skip_aux or not default else {
@@ -798,6 +919,12 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def multi_gpu_unavailable(n):
+    """The line printed instead of a measurement when more than one GPU is asked for."""
+    return {"metric": METRIC, "n_gpus": n, "unavailable":
+            "the GEMMs use cluster-multicast TMA loads: 1-GPU calls only"}
 
 
 def main(argv=None):
@@ -826,7 +953,6 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         if args.workload != WORKLOAD:
             if rank == 0:
@@ -835,17 +961,12 @@ def main(argv=None):
                                   f"({WORKLOAD}) only"}), flush=True)
             return 0
         return reference_arm(args, rank, world)
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    try:
-        return ours_arm(args, rank, world, local_rank)
-    finally:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+    if world > 1 or args.gpus > 1:
+        # nothing is launched: the multicast GEMMs run in single-GPU processes only
+        if rank == 0:
+            print(json.dumps(multi_gpu_unavailable(max(world, args.gpus))), flush=True)
+        return 0
+    return ours_arm(args)
 
 
 if __name__ == "__main__":

@@ -162,5 +162,64 @@ def test_report_line_carries_the_contract_keys(capsys):
     # the dominant kernel is taken among the operations timed alone (gemm_dual here)
     assert roof["kernel"] == "gemm_dual" and roof["bound"] == "tensor"
     assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    # no power-cap share in these clocks: the burst peak, both fractions printed
+    peaks = bench.load_peaks()
+    assert roof["peak"] == peaks["bf16_tflops"] and roof["peak_kind"].endswith("burst")
+    assert roof["frac_burst"] == pytest.approx(roof["achieved"] / peaks["bf16_tflops"])
+    assert roof["frac_sustained"] == pytest.approx(roof["achieved"] /
+                                                   peaks["bf16_tflops_sustained"])
     assert line["gpu_launches"] == 4 * steps + 3 * steps   # kernels, not operations
     assert line["step_ms"]["median"] == pytest.approx(3.7)
+
+
+def test_more_than_one_gpu_prints_unavailable_and_launches_nothing(capsys, monkeypatch):
+    # the GEMMs use cluster-multicast TMA loads, which run in single-GPU processes only:
+    # a request for 2 GPUs (flag or torchrun environment) prints one line and returns 0
+    import json
+
+    monkeypatch.setattr(bench, "ours_arm", lambda *a, **k: pytest.fail("kernels launched"))
+    assert bench.main(["--gpus", "2"]) == 0
+    line = json.loads(capsys.readouterr().out.strip())
+    assert "unavailable" in line and "multicast" in line["unavailable"]
+    assert line["n_gpus"] == 2 and line["metric"] == bench.METRIC
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")                # non-zero ranks print nothing
+    assert bench.main([]) == 0
+    assert capsys.readouterr().out == ""
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main([]) == 0
+    assert json.loads(capsys.readouterr().out.strip())["n_gpus"] == 2
+
+
+def _samples(n_cap, n_free, mhz_cap=1800.0):
+    return ([(mhz_cap, 2070.0, 1390.0, {"sw_power_cap"})] * n_cap +
+            [(2070.0, 2070.0, 900.0, set())] * n_free)
+
+
+def test_peak_follows_the_power_cap_share_of_the_timed_region():
+    peaks = {"bf16_tflops": 1965.5, "bf16_tflops_sustained": 1783.2}
+    # a short region at full clock: burst
+    c = bench.summarize_clocks(_samples(1, 13), "nvml")
+    assert c["power_cap_share"] == pytest.approx(1 / 14) and c["sm_mhz"] == 2070.0
+    assert bench.choose_peak(peaks, c) == ("burst", 1965.5)
+    # capped for most of the region: sustained
+    c = bench.summarize_clocks(_samples(9, 5), "nvml")
+    assert c["sm_mhz"] == 1800.0 and c["reasons"] == ["sw_power_cap"]
+    assert bench.choose_peak(peaks, c) == ("sustained", 1783.2)
+    # exactly half: sustained; no samples at all: burst
+    assert bench.choose_peak(peaks, bench.summarize_clocks(_samples(2, 2), "nvml"))[0] == \
+        "sustained"
+    assert bench.choose_peak(peaks, bench.summarize_clocks([], "nvml")) == ("burst", 1965.5)
+    assert bench.choose_peak(peaks, None) == ("burst", 1965.5)
+
+
+def test_clock_samples_are_taken_from_the_timed_region_only():
+    s = _samples(0, 1)[0]
+    capped = _samples(1, 0)[0]
+    timed = [(0.5, s), (1.0, capped), (1.5, capped), (3.0, s)]
+    c = bench.ClockSampler.select(timed, 0.9, 2.0, "nvml")
+    assert c["samples"] == 2 and c["power_cap_share"] == 1.0 and c["sm_mhz"] == 1800.0
+    # nothing inside: the sample nearest the region's middle, flagged
+    c = bench.ClockSampler.select(timed, 2.4, 2.8, "nvml")
+    assert c["samples"] == 0 and "note" in c and c["sm_mhz"] == 2070.0
+    assert bench.ClockSampler.select([], 0.0, 1.0, "nvml")["samples"] == 0
