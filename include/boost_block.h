@@ -201,8 +201,10 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x,
  * (a direct allocation would bypass its accounting or fail under its memory cap)
  * and plugins that are handed only their input and output buffers.
  *   x     [T, d]   input activations (device)
- *   rstd  [T] fp32 out: (sum_s ssq[s,t] / d + eps)^-1/2, the same value
- *                  boost_rmsnorm_stats returns; desc->has_norm must be 1
+ *   rstd  [T] fp32 out: (sum_s ssq[s,t] / d + eps)^-1/2, shards summed in index
+ *                  order; equal to boost_rmsnorm_stats's rstd up to fp32 rounding
+ *                  (its kernels split a row among threads differently, so the
+ *                  partial sums are added in another order); desc->has_norm must be 1
  * The S x T per-shard partials live in one fixed array of 2^20 floats (4 MiB)
  * inside the library, reserved on every GPU that loads it and held until the
  * process exits. Limit: S*T <= 1048576, else BOOST_ERR_UNSUPPORTED_SHAPE and

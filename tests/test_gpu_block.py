@@ -48,6 +48,74 @@ def test_rmsnorm_stats_parity(T, d, S):
     np.testing.assert_allclose(to_np(rstd), o_rstd, rtol=2e-6, atol=0)
 
 
+# ---------------------------------------------------------------- edge rows
+#
+# Rows the statistics and the RMSNorm-backward epilogue must survive: an all-zero row
+# (rstd = eps^-1/2), constant rows (closed form (c^2 + eps)^-1/2), rows scaled to
+# |x| ~ 1e3 and a row with a single non-zero value, planted among ordinary rows.
+
+EDGE_C = (3.0, -0.5)        # constants, exact in bf16; c^2 * (d / S) is exact in fp32
+
+
+def _edge_x(T, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, d, generator=g)
+    x[0] = 0.0
+    x[1] = EDGE_C[0]
+    x[2] = EDGE_C[1]
+    x[3:6] *= 1000.0
+    x[6] = 0.0
+    x[6, d // 2] = 7.0
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("T,d,S", [(64, 256, 4), (40, 48, 16), (300, 4096, 8)])
+def test_rmsnorm_stats_edge_rows(T, d, S):
+    x = _edge_x(T, d, seed=T)
+    eps = 1e-5
+    desc = B.make_desc(T, d, 8, 1, 8, S=S, eps=eps)
+    ssq, rstd = B.rmsnorm_stats(desc, x.cuda())
+    torch.cuda.synchronize()
+    ssq, rstd = to_np(ssq), to_np(rstd)
+    # closed forms: exact sums of squares, rstd to fp32 precision
+    assert np.all(ssq[:, 0] == 0.0)
+    assert rstd[0] == pytest.approx(eps ** -0.5, rel=1e-6)
+    for row, c in ((1, EDGE_C[0]), (2, EDGE_C[1])):
+        assert np.all(ssq[:, row] == c * c * (d // S))
+        assert rstd[row] == pytest.approx((c * c + eps) ** -0.5, rel=1e-6)
+    assert ssq[:, 6].sum() == 49.0 and rstd[6] == pytest.approx((49.0 / d + eps) ** -0.5,
+                                                                 rel=1e-6)
+    # and everything against the oracle
+    o_ssq, o_rstd = oracle.rmsnorm_stats(inputs.as_f64(x), S, eps)
+    np.testing.assert_allclose(ssq, o_ssq, rtol=2e-5, atol=1e-6)
+    np.testing.assert_allclose(rstd, o_rstd, rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("T,d,r,k,n,S", [(300, 256, 64, 3, 256, 4), (4352, 512, 512, 2, 1024, 4)])
+def test_block_with_edge_rows(T, d, r, k, n, S):
+    # the second shape takes the benchmarked launch shapes (2 x 2 clusters, co-scheduled
+    # rows): the planted rows sit in the cluster launch's first tile
+    w = inputs.make_block(T, d, r, k, n, seed=21)
+    w["x"] = _edge_x(T, d, seed=22)
+    blk = Block(T, d, r, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    blk.forward(x)
+    blk.backward(x, dy)
+    B.check(blk.ws)
+    y, c, gr = oracle_block(w, act="silu", has_norm=True, S=S)
+    assert torch.count_nonzero(blk.y[:, 0]) == 0          # silu(0) = 0 through B: zero
+    np.testing.assert_allclose(to_np(blk.rstd), c["s"], rtol=2e-6)
+    assert_close("y", blk.y, y)
+    assert_close("dx", blk.dx, gr["dx"])
+    assert_close("dA", blk.dA, gr["dA"])
+    assert_close("dB", blk.dB, gr["dB"])
+    assert_close("dgamma", blk.dgamma, gr["dgamma"])
+    # the edge rows on their own (a row's dx is that row's business alone)
+    rows = slice(0, 7)
+    assert_close("y edge rows", blk.y[:, rows], y[:, rows])
+    assert_close("dx edge rows", blk.dx[rows], gr["dx"][rows])
+
+
 # ------------------------------------------------------------------- blocks
 
 CASES = [

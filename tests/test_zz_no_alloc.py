@@ -3,18 +3,21 @@ cudaMalloc (code under a host framework whose allocator owns the device memory,
 plugins handed only their input and output buffers).
 
 It keeps the per-shard partials in one fixed array inside the library, shared
-by every call, so two calls in a row with different shapes must each give the
-row scales the regular statistics entry point gives: the second call may not
-read anything the first one left behind. This file is collected last.
+by every call, so calls in a row with different shapes must each give the row
+scales the regular statistics entry point gives, and the oracle's: a later call
+may not read anything an earlier one left behind. This file is collected last.
 """
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from rank_bottleneck_online_gb300 import binding as B
 from rank_bottleneck_online_gb300 import build as build_mod
+from rank_bottleneck_online_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -27,17 +30,25 @@ def _lib():
     B.lib()
 
 
-def test_noalloc_rstd_matches_regular_entry_point_on_two_calls():
+def test_noalloc_rstd_matches_regular_entry_point_and_oracle_on_calls_in_a_row():
     g = torch.Generator().manual_seed(11)
-    # the second call is smaller and differently sharded than the first, so stale
-    # partials from the first call sit in the shared array during the second
-    for T, d, S in [(4096, 4096, 8), (333, 264, 3)]:
-        x = (torch.randn(T, d, generator=g) * 1.5).to(torch.bfloat16).cuda()
+    # Each call is smaller and differently sharded than the one before, so stale
+    # partials from earlier calls sit in the shared array. The last shape has a shard
+    # width of 3 columns (d % 8 == 0 but (d / S) % 8 != 0): the scalar path of the
+    # partials kernel.
+    for T, d, S in [(4096, 4096, 8), (333, 264, 3), (257, 48, 16)]:
+        x = (torch.randn(T, d, generator=g) * 1.5).to(torch.bfloat16)
+        xd = x.cuda()
         desc = B.make_desc(T, d, 8, 1, 8, S=S, eps=1e-5)
-        _, want = B.rmsnorm_stats(desc, x)
-        got = B.rmsnorm_rstd_noalloc(desc, x)
+        _, want = B.rmsnorm_stats(desc, xd)
+        got = B.rmsnorm_rstd_noalloc(desc, xd)
         torch.cuda.synchronize()
+        # the regular entry point adds the same squares in another per-thread order:
+        # equal up to fp32 rounding
         torch.testing.assert_close(got, want, rtol=2e-6, atol=0)
+        # the oracle (fp64): fp32 accumulation of d squares, then the square root
+        _, s_ref = oracle.rmsnorm_stats(inputs.as_f64(x), S, 1e-5)
+        np.testing.assert_allclose(got.double().cpu().numpy(), s_ref, rtol=1e-5, atol=0)
 
 
 def test_noalloc_rejects_sizes_beyond_the_fixed_array():
