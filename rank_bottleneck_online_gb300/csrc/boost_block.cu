@@ -957,6 +957,10 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
   static const int tma_dual_max_k = env_int("BOOST_TMA_DUAL_MAX_K", 4096);
   const bool dual_tma = P.d + P.n <= tma_dual_max_k;
   if (dual_tma) set_out_maps(g, P.T, P.kr, 1, 1);
+  // rows of super-tiles per group of a grouped raster order (m fastest within a group);
+  // 0 or 1: n fastest
+  static const int dual_m_group = env_int("BOOST_DUAL_MGROUP", 0);
+  g.m_group = dual_m_group;
   cudaError_t e;
   {
     ProfScope ps(s, K_DUAL, 2.0 * P.T * P.kr * (P.d + P.n),
@@ -1076,6 +1080,8 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.out = dgate;
       w.out2 = dup;
       set_out_maps(w, P.T, P.d, 1, 1);
+      // the SwiGLU backward stores dgate and dup only through these maps
+      if (w.tma_out != 3) return BOOST_ERR_CUDA;
       // the epilogue streams gate and up through TMA (required by this mode)
       if (!make_map(&w.tmE[0], gate, P.d, P.T, 1, P.d * 2, P.T * P.d * 2, 32, 32, 1, true) ||
           !make_map(&w.tmE[1], up, P.d, P.T, 1, P.d * 2, P.T * P.d * 2, 32, 32, 1, true))

@@ -60,6 +60,11 @@ constexpr int kEpiHalves = kEpiWarps / 4;
 #ifndef BOOST_GLU_EPI_WARPS
 #define BOOST_GLU_EPI_WARPS 8
 #endif
+// SwiGLU backward: outputs written over their own inputs in the loader's slots (two
+// slots per warp, no separate store ring); 0 keeps one input slot and two store slots.
+#ifndef BOOST_GLU_IN_PLACE
+#define BOOST_GLU_IN_PLACE 1
+#endif
 constexpr int kGluEpiWarps = BOOST_GLU_EPI_WARPS;
 
 enum EpiMode : int {
@@ -163,11 +168,16 @@ struct GemmCfg {
   // the shared memory a second slot takes costs the mainloop a pipeline stage, and these
   // short-K GEMMs with heavy epilogue traffic need the deeper operand pipeline more.
   static constexpr int kEpiStreams = (MODE == EPI_GLU) ? 2 : (MODE == EPI_DX ? 1 : 0);
-  static constexpr int kEpiDepth = 1;
+  // EPI_GLU in place: each warp's gate/up slot also holds the chunk's dgate/dup for their
+  // TMA stores, so the shared memory of the store ring buys a second input slot instead:
+  // the loads run two chunks ahead of the consumer (each slot is reloaded as soon as the
+  // stores from it have read it).
+  static constexpr bool kInPlace = (MODE == EPI_GLU) && BOOST_GLU_IN_PLACE;
+  static constexpr int kEpiDepth = kInPlace ? 2 : 1;
   // Staging per warp: load slots (the loader's kEpiDepth x kEpiStreams 2 KB slots, or one
   // 2 KB slot for EPI_DA's synchronous loads), then the store slots (2 KB each); fp32
   // partials use one 4 KB block.
-  static constexpr int kStoreSlots = (MODE == EPI_F32) ? 0 : (kTmaStore ? 2 : 1);
+  static constexpr int kStoreSlots = (MODE == EPI_F32 || kInPlace) ? 0 : (kTmaStore ? 2 : 1);
   static constexpr int kLoadBytes =
       kEpiStreams > 0 ? kEpiDepth * kEpiStreams * 2048 : (MODE == EPI_DA ? 2048 : 0);
   static constexpr int kWarpStg = (MODE == EPI_F32) ? 4096 : kLoadBytes + 2048 * kStoreSlots;
@@ -467,8 +477,10 @@ __device__ __forceinline__ void slot_row_f32(const uint8_t* slot, int lane, floa
 // kDepth slots, kDepth chunks ahead of the consumer. The loads do not depend on the
 // accumulator, so the next tile's first chunks are in flight before its MMAs finish.
 // Lane 0 issues; every lane waits on the slot's mbarrier (bounded) before reading.
-template <int BN, int TILE_N, int TILE_M, int kStreams, int kDepth, int kHalves>
+template <int BN, int TILE_N, int TILE_M, int kStreams, int kDepth, int kHalves,
+          bool kInPlaceUse = false>
 struct EpiLoader {
+  static constexpr bool kInPlace = kInPlaceUse;
   static constexpr int kChunks = (BN / 32 + kHalves - 1) / kHalves;   // most chunks a warp takes
   // gate and up of the SwiGLU backward are read once: keep them from displacing operands
   static constexpr bool kEvictFirst = (kStreams == 2);
@@ -535,6 +547,24 @@ struct EpiLoader {
     issue_next(lane);
   }
 
+  // In-place use: wait for the warp's next chunk and return its slot (tensor t at
+  // + t * 2 KB, 64-byte swizzled rows). The caller overwrites the slot with its outputs,
+  // stores them from it and then calls refill().
+  __device__ __forceinline__ uint8_t* wait_slot() {
+    const uint32_t slot = consumed % kDepth;
+    bounded_wait(&bars[slot], (consumed / kDepth) & 1u, p->err, 9, p->wait_limit_ns);
+    ++consumed;
+    return slots + slot * kSlotBytes;
+  }
+
+  // In-place use: once this warp's stores have read the slot just consumed (lane 0 issued
+  // and committed them), load the chunk kDepth ahead into it.
+  __device__ __forceinline__ void refill(int lane) {
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    issue_next(lane);
+  }
+
   // Wait for loads still in flight (only after an early exit from the tile loop).
   __device__ __forceinline__ void drain() {
     while (consumed < issued) {
@@ -547,6 +577,7 @@ struct EpiLoader {
 
 // Stand-in for modes without streamed inputs.
 struct NoLoader {
+  static constexpr bool kInPlace = false;
   __device__ __forceinline__ void start(int) {}
   __device__ __forceinline__ void drain() {}
 };
@@ -559,6 +590,68 @@ __device__ __forceinline__ void count_writes(const GemmParams& p, int64_t base, 
     int32_t* v = p.visits + base + static_cast<int64_t>(lane) * p.ldo;
     for (int c = 0; c < 32 && c < cols_valid; ++c) atomicAdd(v + c, 1);
   }
+}
+
+// SwiGLU backward of two adjacent columns: the down-projection's input gradient dh (the
+// accumulator pair a0, a1, rounded to bf16 as a separate pass would have stored it) and
+// the bf16 gate and up pairs g2, u2 give dgate = dh * up * silu'(gate) and
+// dup = dh * silu(gate), packed as bf16 pairs.
+__device__ __forceinline__ void glu_pair(float a0, float a1, uint32_t g2, uint32_t u2,
+                                         uint32_t& dgate, uint32_t& dup) {
+  const uint32_t dh2 = pack_bf16x2(a0, a1);   // both rounded in one convert
+  float dgo[2], duo[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float dh = h == 0 ? bf16_lo(dh2) : bf16_hi(dh2);
+    const float z = h == 0 ? bf16_lo(g2) : bf16_hi(g2);
+    const float u = h == 0 ? bf16_lo(u2) : bf16_hi(u2);
+    const float sg = sigmoid_f(z);
+    dgo[h] = dh * u * (sg * (1.0f + z * (1.0f - sg)));
+    duo[h] = dh * (z * sg);
+  }
+  dgate = pack_bf16x2(dgo[0], dgo[1]);
+  dup = pack_bf16x2(duo[0], duo[1]);
+}
+
+// One 32 x 32 chunk of the SwiGLU backward in place (rows [row0, row0 + 32), columns
+// [col0, col0 + 32)): the accumulator (this lane's row) and the chunk's gate and up from
+// the loader's slot give dgate and dup, which each lane writes over its own row of gate
+// and up in the slot (same 64-byte swizzled layout as the output maps); lane 0 stores
+// both with TMA (evict-first in L2: written once) and the loader reloads the slot.
+template <class Loader>
+__device__ __forceinline__ void glu_chunk_in_place(const GemmParams& p, Loader& ld, int lane,
+                                                   uint32_t t_col, int32_t col0, int32_t row0,
+                                                   int rows_valid, int cols_valid) {
+  float v[32];
+  tmem_ld_32x32b_x32(t_col, v);
+  uint8_t* slot = ld.wait_slot();
+  tmem_ld_wait();
+  uint4* gr = reinterpret_cast<uint4*>(slot + lane * 64);
+  uint4* ur = reinterpret_cast<uint4*>(slot + 2048 + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    const uint4 gq = gr[c4 ^ sw], uq = ur[c4 ^ sw];
+    const float* a = v + 8 * c4;
+    uint4 dg, du;
+    glu_pair(a[0], a[1], gq.x, uq.x, dg.x, du.x);
+    glu_pair(a[2], a[3], gq.y, uq.y, dg.y, du.y);
+    glu_pair(a[4], a[5], gq.z, uq.z, dg.z, du.z);
+    glu_pair(a[6], a[7], gq.w, uq.w, dg.w, du.w);
+    gr[c4 ^ sw] = dg;
+    ur[c4 ^ sw] = du;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const uint64_t pol = l2_evict_first();
+    tma_store_3d_hint(&p.tmO[0], slot, col0, row0, 0, pol);
+    tma_store_3d_hint(&p.tmO[1], slot + 2048, col0, row0, 0, pol);
+    bulk_commit_group();
+  }
+  if (p.visits != nullptr)
+    count_writes(p, static_cast<int64_t>(row0) * p.ldo + col0, lane, rows_valid, cols_valid);
+  ld.refill(lane);
 }
 
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
@@ -601,112 +694,116 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     const int32_t col0 = n0 + c * 32;
     const int cols_valid = n_end - col0;
     if (cols_valid <= 0) break;            // warp-uniform: the rest of the tile is outside N
-    const bool whole = cols_valid >= 32 || n_end == p.N;   // the maps clip at N only
-    float v[32];
-    tmem_ld_32x32b_x32(t_row + c * 32, v);
-    float w[32];
-    if constexpr (is_dual(MODE)) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
-    tmem_ld_wait();
-    if constexpr (MODE == EPI_F32) {
-      const int64_t base = tc.split * p.out_sstride + tc.batch * p.out_bstride +
-                           static_cast<int64_t>(row0) * p.ldo + col0;
-      stage_store_f32(stg, lane, v, static_cast<float*>(p.out) + base, p.ldo, rows_valid,
-                      cols_valid);
-      if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
+    if constexpr (MODE == EPI_GLU && Loader::kInPlace) {
+      glu_chunk_in_place(p, ld, lane, t_row + c * 32, col0, row0, rows_valid, cols_valid);
     } else {
-      uint32_t pk[16];
-      if constexpr (MODE == EPI_ACT) {
+      const bool whole = cols_valid >= 32 || n_end == p.N;   // the maps clip at N only
+      float v[32];
+      tmem_ld_32x32b_x32(t_row + c * 32, v);
+      float w[32];
+      if constexpr (is_dual(MODE)) tmem_ld_32x32b_x32(t_row + BN + c * 32, w);
+      tmem_ld_wait();
+      if constexpr (MODE == EPI_F32) {
+        const int64_t base = tc.split * p.out_sstride + tc.batch * p.out_bstride +
+                             static_cast<int64_t>(row0) * p.ldo + col0;
+        stage_store_f32(stg, lane, v, static_cast<float*>(p.out) + base, p.ldo, rows_valid,
+                        cols_valid);
+        if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
+      } else {
+        uint32_t pk[16];
+        if constexpr (MODE == EPI_ACT) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act),
-                              act_fwd(s_row * v[2 * i + 1], p.act));
-      } else if constexpr (MODE == EPI_BF16 || MODE == EPI_BF16T) {
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act),
+                                act_fwd(s_row * v[2 * i + 1], p.act));
+        } else if constexpr (MODE == EPI_BF16 || MODE == EPI_BF16T) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-      } else if constexpr (is_dual(MODE)) {
-        // a = act(z) (recompute) and dzs = s * act'(z) * (dy B^T); row partial of dz * z.
-        uint32_t pk2[16];
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        } else if constexpr (is_dual(MODE)) {
+          // a = act(z) (recompute) and dzs = s * act'(z) * (dy B^T); row partial of dz * z.
+          uint32_t pk2[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float a2[2], d2[2];
+          for (int i = 0; i < 32; i += 2) {
+            float a2[2], d2[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float z = s_row * v[i + h];
-            float dz;
-            if (p.act == 1) {
-              const float sg = sigmoid_f(z);
-              a2[h] = z * sg;
-              dz = w[i + h] * (sg * (1.0f + z * (1.0f - sg)));
-            } else {
-              a2[h] = z;
-              dz = w[i + h];
+            for (int h = 0; h < 2; ++h) {
+              const float z = s_row * v[i + h];
+              float dz;
+              if (p.act == 1) {
+                const float sg = sigmoid_f(z);
+                a2[h] = z * sg;
+                dz = w[i + h] * (sg * (1.0f + z * (1.0f - sg)));
+              } else {
+                a2[h] = z;
+                dz = w[i + h];
+              }
+              if (i + h < cols_valid) rowsum += dz * z;
+              d2[h] = s_row * dz;
             }
-            if (i + h < cols_valid) rowsum += dz * z;
-            d2[h] = s_row * dz;
+            pk[i / 2] = pack_bf16x2(a2[0], a2[1]);
+            pk2[i / 2] = pack_bf16x2(d2[0], d2[1]);
           }
-          pk[i / 2] = pack_bf16x2(a2[0], a2[1]);
-          pk2[i / 2] = pack_bf16x2(d2[0], d2[1]);
-        }
-        __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
-                            static_cast<int64_t>(row0) * p.ldo + col0;
-        store_chunk_bf16(ring, lane, pk2, &p.tmO[1], whole && (p.tma_out & 2), col0, row0, 0, o2,
-                         p.ldo, rows_valid, cols_valid);
-      } else if constexpr (MODE == EPI_GLU) {
-        // SwiGLU backward on the down-projection's input gradient dh (rounded to bf16,
-        // the value a separate pass would have stored): dgate and dup of h = silu(g)*u.
-        float gu[2][32];   // gate, up
-        ld.consume(lane, gu);
-        uint32_t pk2[16];
+          __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
+                              static_cast<int64_t>(row0) * p.ldo + col0;
+          store_chunk_bf16(ring, lane, pk2, &p.tmO[1], whole && (p.tma_out & 2), col0, row0, 0, o2,
+                           p.ldo, rows_valid, cols_valid);
+        } else if constexpr (MODE == EPI_GLU) {
+          // SwiGLU backward on the down-projection's input gradient dh (rounded to bf16,
+          // the value a separate pass would have stored): dgate and dup of h = silu(g)*u.
+          float gu[2][32];   // gate, up
+          ld.consume(lane, gu);
+          uint32_t pk2[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float dgo[2], duo[2];
-          const uint32_t dh2 = pack_bf16x2(v[i], v[i + 1]);   // both rounded in one convert
+          for (int i = 0; i < 32; i += 2) {
+            float dgo[2], duo[2];
+            const uint32_t dh2 = pack_bf16x2(v[i], v[i + 1]);   // both rounded in one convert
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float dh = h == 0 ? bf16_lo(dh2) : bf16_hi(dh2);
-            const float z = gu[0][i + h];
-            const float sg = sigmoid_f(z);
-            dgo[h] = dh * gu[1][i + h] * (sg * (1.0f + z * (1.0f - sg)));
-            duo[h] = dh * (z * sg);
+            for (int h = 0; h < 2; ++h) {
+              const float dh = h == 0 ? bf16_lo(dh2) : bf16_hi(dh2);
+              const float z = gu[0][i + h];
+              const float sg = sigmoid_f(z);
+              dgo[h] = dh * gu[1][i + h] * (sg * (1.0f + z * (1.0f - sg)));
+              duo[h] = dh * (z * sg);
+            }
+            pk[i / 2] = pack_bf16x2(dgo[0], dgo[1]);
+            pk2[i / 2] = pack_bf16x2(duo[0], duo[1]);
           }
-          pk[i / 2] = pack_bf16x2(dgo[0], dgo[1]);
-          pk2[i / 2] = pack_bf16x2(duo[0], duo[1]);
+          __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
+                              static_cast<int64_t>(row0) * p.ldo + col0;
+          // (dgate and dup are written once here: evict-first in L2)
+          store_chunk_bf16<kSlots, kTma, true>(ring, lane, pk2, &p.tmO[1],
+                                               whole && (p.tma_out & 2), col0, row0, 0, o2,
+                                               p.ldo, rows_valid, cols_valid);
+        } else if constexpr (MODE == EPI_DX) {
+          float xv[1][32];
+          if (p.tma_in) {                          // RMSNorm term: x streamed by the loader
+            ld.consume(lane, xv);
+          } else {                                 // no norm: coef == 0
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xv[0][i] = 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(v[2 * i] - coef * xv[0][2 * i],
+                                v[2 * i + 1] - coef * xv[0][2 * i + 1]);
+        } else if constexpr (MODE == EPI_DA) {
+          if (p.wA != nullptr) {
+            float av[32];
+            stage_load_bf16(stg, lane, p.wA + static_cast<int64_t>(row0) * p.ldo + col0, p.ldo,
+                            rows_valid, cols_valid, av);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rowsum += av[i] * v[i];
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
         }
-        __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
-                            static_cast<int64_t>(row0) * p.ldo + col0;
-        // (dgate and dup are written once here: evict-first in L2)
-        store_chunk_bf16<kSlots, kTma, true>(ring, lane, pk2, &p.tmO[1],
-                                             whole && (p.tma_out & 2), col0, row0, 0, o2,
-                                             p.ldo, rows_valid, cols_valid);
-      } else if constexpr (MODE == EPI_DX) {
-        float xv[1][32];
-        if (p.tma_in) {                          // RMSNorm term: x streamed by the loader
-          ld.consume(lane, xv);
-        } else {                                 // no norm: coef == 0
-#pragma unroll
-          for (int i = 0; i < 32; ++i) xv[0][i] = 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(v[2 * i] - coef * xv[0][2 * i],
-                              v[2 * i + 1] - coef * xv[0][2 * i + 1]);
-      } else if constexpr (MODE == EPI_DA) {
-        if (p.wA != nullptr) {
-          float av[32];
-          stage_load_bf16(stg, lane, p.wA + static_cast<int64_t>(row0) * p.ldo + col0, p.ldo,
-                          rows_valid, cols_valid, av);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rowsum += av[i] * v[i];
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
+        const int64_t base = tc.batch * p.out_bstride + static_cast<int64_t>(row0) * p.ldo + col0;
+        store_chunk_bf16<kSlots, kTma, MODE == EPI_GLU>(
+            ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
+            static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
+        if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
       }
-      const int64_t base = tc.batch * p.out_bstride + static_cast<int64_t>(row0) * p.ldo + col0;
-      store_chunk_bf16<kSlots, kTma, MODE == EPI_GLU>(
-          ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
-          static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
-      if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
     }
   }
   if constexpr (is_dual(MODE)) {
@@ -1064,7 +1161,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
     constexpr int kStreams = Cfg::kEpiStreams > 0 ? Cfg::kEpiStreams : 1;
     using Loader = typename std::conditional<
         (Cfg::kEpiStreams > 0),
-        EpiLoader<BN, Cfg::kTileN, Cfg::kTileM, kStreams, Cfg::kEpiDepth, Cfg::kHalves>,
+        EpiLoader<BN, Cfg::kTileN, Cfg::kTileM, kStreams, Cfg::kEpiDepth, Cfg::kHalves,
+                  Cfg::kInPlace>,
         NoLoader>::type;
     Loader ld{};
     if constexpr (Cfg::kEpiStreams > 0) {
