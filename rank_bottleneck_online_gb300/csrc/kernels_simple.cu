@@ -175,21 +175,33 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_stats_wide_kernel(
 }
 
 // A'[j, m] = bf16(gamma_j * A[j, m]); the product of two bf16 values is exact in fp32.
-// Grid (column blocks, row blocks): rows j = blockIdx.y, blockIdx.y + gridDim.y, ...;
-// one 16-byte piece of the row per thread.
+// A grid-stride loop over the 16-byte pieces of A; each thread has kFoldUnroll pieces
+// (kThreads pieces apart) in flight before it scales and stores them.
+constexpr int kFoldUnroll = 4;
+
 __global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
-    const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
-    __nv_bfloat16* __restrict__ Ap, int64_t d, int64_t kr) {
-  const int64_t v = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  if (v >= kr / 8) return;
-  for (int64_t j = blockIdx.y; j < d; j += gridDim.y) {
-    const float g = __bfloat162float(gamma[j]);
-    const int64_t i = j * (kr / 8) + v;
-    float f[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(A) + i), f);
+    const __nv_bfloat16* __restrict__ gamma, const uint4* __restrict__ A, uint4* __restrict__ Ap,
+    int64_t nvec, int64_t row_vecs) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * kFoldUnroll;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kFoldUnroll + threadIdx.x;
+       base < nvec; base += stride) {
+    uint4 u[kFoldUnroll];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] *= g;
-    reinterpret_cast<uint4*>(Ap)[i] = pack8(f);
+    for (int k = 0; k < kFoldUnroll; ++k) {
+      const int64_t i = base + k * kThreads;
+      if (i < nvec) u[k] = __ldg(A + i);
+    }
+#pragma unroll
+    for (int k = 0; k < kFoldUnroll; ++k) {
+      const int64_t i = base + k * kThreads;
+      if (i >= nvec) break;
+      const float g = __bfloat162float(gamma[i / row_vecs]);
+      float f[8];
+      unpack8(u[k], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] *= g;
+      Ap[i] = pack8(f);
+    }
   }
 }
 
@@ -238,15 +250,26 @@ __global__ void __launch_bounds__(kThreads) add_kernel(const uint4* a, const uin
   }
 }
 
-// out = bf16(sum_s part[s]) over `count` elements, splits summed in index order.
+// Most split-K splits the host plans (its planner stops at 8).
+constexpr int kMaxSplits = 8;
+
+// out = bf16(sum_s part[s]) over `count` elements, splits summed in index order. Every
+// split's value is loaded before the sum, so a thread has all its loads in flight at once
+// (MAXS: the most splits this instantiation takes, 4 or kMaxSplits).
+template <int MAXS>
 __global__ void __launch_bounds__(kThreads) splitk_sum_bf16_kernel(
     const float4* __restrict__ part, int splits, int64_t count4, uint2* __restrict__ out) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < count4;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
-    float4 acc = part[i];
-    for (int s = 1; s < splits; ++s) {
-      const float4 v = part[static_cast<int64_t>(s) * count4 + i];
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    float4 v[MAXS];
+#pragma unroll
+    for (int s = 0; s < MAXS; ++s)
+      if (s < splits) v[s] = __ldg(part + static_cast<int64_t>(s) * count4 + i);
+    float4 acc = v[0];
+#pragma unroll
+    for (int s = 1; s < MAXS; ++s) {
+      if (s >= splits) break;
+      acc.x += v[s].x; acc.y += v[s].y; acc.z += v[s].z; acc.w += v[s].w;
     }
     out[i] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
@@ -255,7 +278,9 @@ __global__ void __launch_bounds__(kThreads) splitk_sum_bf16_kernel(
 // One block per row j of G = sum_s part[s] ([d, kr], splits summed in order): dA =
 // bf16(gamma_j * G[j, :]) and dgamma_j = bf16(sum_m A[j, m] * G[j, m]), the row sum
 // reduced in a fixed order (per thread, then per warp, then over the warps). Without
-// gamma: dA = bf16(G). Each thread takes 8 columns at a time.
+// gamma: dA = bf16(G). Each thread takes 8 columns at a time (MAXS: the most splits this
+// instantiation takes, 4 or kMaxSplits).
+template <int MAXS>
 __global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
     const float* __restrict__ part, int splits, int64_t d, int64_t kr,
     const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
@@ -269,16 +294,31 @@ __global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
   float acc = 0.0f;
   for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
     const int64_t off = j * kr + i * 8;
-    float G[8];
-    const float4 a0 = __ldg(reinterpret_cast<const float4*>(part + off));
-    const float4 a1 = __ldg(reinterpret_cast<const float4*>(part + off + 4));
-    G[0] = a0.x; G[1] = a0.y; G[2] = a0.z; G[3] = a0.w;
-    G[4] = a1.x; G[5] = a1.y; G[6] = a1.z; G[7] = a1.w;
-    for (int sp = 1; sp < splits; ++sp) {
-      const float4 b0 = __ldg(reinterpret_cast<const float4*>(part + sp * plane + off));
-      const float4 b1 = __ldg(reinterpret_cast<const float4*>(part + sp * plane + off + 4));
-      G[0] += b0.x; G[1] += b0.y; G[2] += b0.z; G[3] += b0.w;
-      G[4] += b1.x; G[5] += b1.y; G[6] += b1.z; G[7] += b1.w;
+    // four splits' 8 values at a time in flight before they are added (splits summed in
+    // index order)
+    float G[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int s0 = 0; s0 < MAXS; s0 += 4) {
+      if (s0 >= splits) break;
+      float4 b[4][2];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (s0 + q < splits) {
+          b[q][0] = __ldg(reinterpret_cast<const float4*>(part + (s0 + q) * plane + off));
+          b[q][1] = __ldg(reinterpret_cast<const float4*>(part + (s0 + q) * plane + off + 4));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (s0 + q >= splits) break;
+        if (s0 + q == 0) {
+          G[0] = b[0][0].x; G[1] = b[0][0].y; G[2] = b[0][0].z; G[3] = b[0][0].w;
+          G[4] = b[0][1].x; G[5] = b[0][1].y; G[6] = b[0][1].z; G[7] = b[0][1].w;
+        } else {
+          G[0] += b[q][0].x; G[1] += b[q][0].y; G[2] += b[q][0].z; G[3] += b[q][0].w;
+          G[4] += b[q][1].x; G[5] += b[q][1].y; G[6] += b[q][1].z; G[7] += b[q][1].w;
+        }
+      }
     }
     float o[8];
     if (gamma != nullptr) {
@@ -377,11 +417,10 @@ cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64
 cudaError_t launch_fold_gamma(const void* gamma, const void* A, void* Ap, int64_t d, int64_t kr,
                               cudaStream_t stream) {
   if (d * kr == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((kr / 8 + kThreads - 1) / kThreads),
-                  static_cast<unsigned>(d < 65535 ? d : 65535));
-  fold_gamma_kernel<<<grid, kThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(A),
-      static_cast<__nv_bfloat16*>(Ap), d, kr);
+  const int64_t nvec = d * (kr / 8);
+  fold_gamma_kernel<<<grid_for(nvec, kThreads * kFoldUnroll), kThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(gamma), static_cast<const uint4*>(A),
+      static_cast<uint4*>(Ap), nvec, kr / 8);
   return cudaGetLastError();
 }
 
@@ -414,8 +453,10 @@ cudaError_t launch_add(const void* a, const void* b, void* out, int64_t count,
 
 cudaError_t launch_splitk_sum_bf16(const float* part, int splits, int64_t count, void* out,
                                    cudaStream_t stream) {
+  if (splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;
   if (count == 0) return cudaSuccess;
-  splitk_sum_bf16_kernel<<<grid_for(count / 4, kThreads), kThreads, 0, stream>>>(
+  const auto kern = splits <= 4 ? splitk_sum_bf16_kernel<4> : splitk_sum_bf16_kernel<kMaxSplits>;
+  kern<<<grid_for(count / 4, kThreads), kThreads, 0, stream>>>(
       reinterpret_cast<const float4*>(part), splits, count / 4, static_cast<uint2*>(out));
   return cudaGetLastError();
 }
@@ -423,8 +464,11 @@ cudaError_t launch_splitk_sum_bf16(const float* part, int splits, int64_t count,
 cudaError_t launch_splitk_finalize_dA(const float* part, int splits, int64_t d, int64_t kr,
                                       const void* gamma, const void* A, void* dA, void* dgamma,
                                       cudaStream_t stream) {
+  if (splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;
   if (d == 0) return cudaSuccess;
-  splitk_finalize_dA_kernel<<<static_cast<unsigned>(d), kThreads, 0, stream>>>(
+  const auto kern =
+      splits <= 4 ? splitk_finalize_dA_kernel<4> : splitk_finalize_dA_kernel<kMaxSplits>;
+  kern<<<static_cast<unsigned>(d), kThreads, 0, stream>>>(
       part, splits, d, kr, static_cast<const __nv_bfloat16*>(gamma),
       static_cast<const __nv_bfloat16*>(A), static_cast<__nv_bfloat16*>(dA),
       static_cast<__nv_bfloat16*>(dgamma));
