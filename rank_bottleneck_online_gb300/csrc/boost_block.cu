@@ -431,26 +431,29 @@ CoStreams* co_streams() {
 }
 
 // Launch one GEMM over its M rows; with co-scheduling enabled and a 2 x 2 cluster shape,
-// split the rows between that launch and a CTA-pair launch on a side stream.
+// split the rows between that launch and a CTA-pair launch on a side stream. By default
+// the side launch takes 130 of every 1000 rows (rounded to whole super-tiles of the
+// cluster launch), the best single setting measured over the LLaMA-2 shapes. A planned
+// split replaces it where it is predicted to save at least 2%: the split minimising the
+// larger of the two launches' wave counts, a pair's 256 x 256 tile costing `cost`
+// cluster super-tile waves (the side SMs' pairs have no multicast partner and share L2
+// with the cluster launch, which costs them most where the tiles' K is short: 1.25 at
+// K >= 12288, 1.5 at K >= 1024, 2 below, fitted to per-GEMM timings of the 7B MLP, the 1B
+// block and the 40B pair against fixed splits). On the 7B MLP this moves the gate/up
+// dual kernel, the fused up-projection and the SwiGLU backward to 26-27 cluster rows
+// (2-3% faster each); the 1B block keeps the fixed split everywhere. BOOST_COSCHED_ROWCOST sets one cost (percent) for every K;
+// BOOST_COSCHED > 0 fixes the side launch's rows per 1000 (no planning), 0 turns the
+// split off.
 cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g_in, int sms,
                              cudaStream_t s) {
   GemmParams g = g_in;
   attach_counts(g, mode);
-  // rows of the side launch per 1000; 0 turns co-scheduling off. 130 measured best over
-  // the LLaMA-2 shapes (7B MLP: 130 = 160 > 100; 1B attention block: 130 > 100 > 160):
-  // the 32 leftover SMs run pair tiles at roughly three quarters of the per-SM rate of
-  // the 8-CTA clusters.
-  static const int permille = env_int("BOOST_COSCHED", 130);
+  static const int permille = env_int("BOOST_COSCHED", -1);
+  static const int row_cost_pct = env_int("BOOST_COSCHED_ROWCOST", 0);
   const int64_t M = g.M;
   const int64_t unit = sh.super_m();
-  if (permille <= 0 || sh.mcm * sh.mcn < 4 || M < 8 * unit)
+  if (permille == 0 || sh.mcm * sh.mcn < 4 || M < 8 * unit)
     return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
-  CoStreams* cs = co_streams();
-  if (cs == nullptr) return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
-  int64_t side_rows = M * permille / 1000 / 256 * 256;
-  if (side_rows <= 0) return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
-  const int64_t main_rows = cdiv(M - side_rows, unit) * unit;
-  side_rows = M - main_rows;
   GemmParams a = g, b = g;
   // the side launch tiles N by single pairs (BN wide); group-aligned because a 2 x 2
   // grouped shape requires groups of a multiple of 512 columns
@@ -460,10 +463,52 @@ cudaError_t launch_gemm_rows(const Shape& sh, int mode, const GemmParams& g_in, 
   } else {
     b.n_tiles = static_cast<int32_t>(cdiv(g.N, sh.bn));
   }
+  auto fixed_split = [&](int64_t pm) {
+    const int64_t side_rows = M * pm / 1000 / 256 * 256;
+    return side_rows > 0 ? std::min(M, cdiv(M - side_rows, unit) * unit) : M;
+  };
+  int64_t main_rows = fixed_split(permille > 0 ? permille : 130);
+  if (permille < 0) {
+    const int64_t r_main = gemm_resident(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, sms);
+    const int64_t r_side = (sms - r_main * sh.cg * sh.mcm * sh.mcn) / 2;
+    if (r_main > 0 && r_side > 0) {
+      int64_t k_tile = 0;   // K of one tile, over its segments (one split's share)
+      for (int sg = 0; sg < g.num_seg; ++sg)
+        k_tile += static_cast<int64_t>(g.splits > 1 ? g.kb_per_split : g.seg[sg].num_kb) * kBK;
+      const int pct = row_cost_pct > 0 ? row_cost_pct
+                                       : (k_tile >= 12288 ? 125 : (k_tile >= 1024 ? 150 : 200));
+      const double cost = pct / 100.0;
+      const int64_t units = static_cast<int64_t>(g.batch) * std::max<int32_t>(g.splits, 1);
+      // predicted time (cluster waves) of a split keeping `rows` rows in the cluster launch
+      auto waves = [&](int64_t rows) {
+        const int64_t side = M - rows;
+        const double t_main =
+            static_cast<double>(cdiv(units * cdiv(rows, unit) * a.n_tiles, r_main));
+        const double t_side =
+            side > 0 ? static_cast<double>(cdiv(units * cdiv(side, 256) * b.n_tiles, r_side)) * cost
+                     : 0.0;
+        return std::max(t_main, t_side);
+      };
+      double best = 1e300;
+      int64_t best_rows = main_rows;
+      for (int64_t i = cdiv(M, unit); i * unit * 2 >= M; --i) {
+        const int64_t rows = std::min(i * unit, M);
+        const double t = waves(rows);
+        if (t < best * 0.999) {
+          best = t;
+          best_rows = rows;
+        }
+      }
+      if (best < 0.98 * waves(main_rows)) main_rows = best_rows;
+    }
+  }
+  if (main_rows >= M) return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
+  CoStreams* cs = co_streams();
+  if (cs == nullptr) return launch_gemm(sh.bn, mode, sh.cg, sh.mcm, sh.mcn, g, sms, s);
   a.m_base = 0;
   a.m_extent = static_cast<int32_t>(main_rows);
   b.m_base = static_cast<int32_t>(main_rows);
-  b.m_extent = static_cast<int32_t>(side_rows);
+  b.m_extent = static_cast<int32_t>(M - main_rows);
   std::lock_guard<std::mutex> lk(cs->order);
   cudaError_t e = cudaEventRecord(cs->fork, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->side, cs->fork, 0);

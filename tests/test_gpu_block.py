@@ -175,9 +175,11 @@ def test_recompute_is_bitwise_equal_to_forward(case):
 @pytest.mark.skipif(os.environ.get("BOOST_COSCHED", "") == "0",
                     reason="co-scheduling turned off in the environment")
 def test_co_scheduled_gemms_count_two_kernels():
-    # T = 4352 rows take the split launch shape for every GEMM over the token rows;
-    # the profiler counts one timed operation and two kernels for each of them
-    T, d, r, k, n, S = 4352, 512, 512, 2, 1024, 4
+    # T = 8448 rows (16.5 rows of 512-row super-tiles) take the split launch shape for
+    # every GEMM over the token rows, whether the split is planned from the launches' wave
+    # counts or fixed per 1000 rows; the profiler counts one timed operation and two
+    # kernels for each of them
+    T, d, r, k, n, S = 8448, 512, 512, 2, 1024, 4
     w = inputs.make_block(T, d, r, k, n, seed=6)
     blk = Block(T, d, r, k, n, S=S, weights=w)
     x, dy = w["x"].cuda(), w["dy"].cuda()
