@@ -34,6 +34,7 @@ EXPORTS = (
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
     "boost_profile_read_kernels", "boost_block_fwd_swiglu", "boost_block_fwd_btp",
     "boost_block_up", "boost_debug_count_writes", "boost_debug_count_log",
+    "boost_profile_only",
 )
 
 
@@ -93,6 +94,7 @@ def lib():
     L.boost_rmsnorm_rstd_noalloc.argtypes = [dp, vp, vp, vp]
     L.boost_block_bwd_swiglu.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.boost_profile_enable.argtypes = [ctypes.c_int]
+    L.boost_profile_only.argtypes = [ctypes.c_int]
     L.boost_profile_kernel_count.argtypes = []
     dbl = ctypes.POINTER(ctypes.c_double)
     L.boost_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
@@ -412,6 +414,23 @@ def check(ws: Workspace, stream=None):
 
 def profile_enable(on: bool):
     _check(lib().boost_profile_enable(1 if on else 0), "boost_profile_enable")
+
+
+def profile_only(name=None):
+    """Time only the named kernel's operations (None: every kernel)."""
+    L = lib()
+    idx = -1
+    if name is not None:
+        names = {}
+        for i in range(L.boost_profile_kernel_count()):
+            nm = ctypes.c_char_p()
+            _check(L.boost_profile_read(i, ctypes.byref(nm), None, None, None, None),
+                   "boost_profile_read")
+            names[nm.value.decode()] = i
+        if name not in names:
+            raise KeyError(name)
+        idx = names[name]
+    _check(L.boost_profile_only(idx), "boost_profile_only")
 
 
 def profile_kernels():

@@ -1,7 +1,7 @@
 // profile.cu -- optional per-kernel timing of the library's own launches.
 //
-// When enabled, every kernel launch is bracketed by two CUDA events recorded on
-// the launch's stream, and the launch's algorithmic work (flops and bytes, from the
+// When enabled, every kernel launch (or, with boost_profile_only, every launch of one
+// kernel) is bracketed by two CUDA events recorded on the launch's stream, and the launch's algorithmic work (flops and bytes, from the
 // shapes) is accumulated per kernel. Reading the counters synchronises the pending
 // events. Disabled (the default), a launch pays one relaxed atomic load. While the
 // stream is being captured into a CUDA graph the events become event-record nodes of
@@ -37,6 +37,7 @@ struct Totals {
 };
 
 std::atomic<int> g_enabled{0};
+std::atomic<int> g_only{-1};   // the one kernel id timed, or -1 for all
 std::mutex g_mu;
 std::vector<Pending> g_pending;
 std::vector<cudaEvent_t> g_pool;
@@ -90,6 +91,8 @@ void record(cudaEvent_t e, cudaStream_t s) {
 ProfScope::ProfScope(cudaStream_t s, int id, double flops, double bytes)
     : stream_(s), id_(id), flops_(flops), bytes_(bytes) {
   if (g_enabled.load(std::memory_order_relaxed) == 0) return;
+  const int only = g_only.load(std::memory_order_relaxed);
+  if (only >= 0 && only != id) return;
   std::lock_guard<std::mutex> lk(g_mu);
   e0_ = take_event();
   e1_ = take_event();
@@ -126,6 +129,12 @@ boost_status boost_profile_enable(int on) {
     for (auto& t : g_tot) t = Totals{};
   }
   g_enabled.store(on ? 1 : 0);
+  return BOOST_OK;
+}
+
+boost_status boost_profile_only(int id) {
+  if (id < -1 || id >= K_COUNT) return BOOST_ERR_INVALID_ARG;
+  g_only.store(id);
   return BOOST_OK;
 }
 

@@ -223,3 +223,23 @@ def test_clock_samples_are_taken_from_the_timed_region_only():
     c = bench.ClockSampler.select(timed, 2.4, 2.8, "nvml")
     assert c["samples"] == 0 and "note" in c and c["sm_mhz"] == 2070.0
     assert bench.ClockSampler.select([], 0.0, 1.0, "nvml")["samples"] == 0
+
+
+def test_roofline_takes_the_dominant_kernel_timed_in_the_timed_region(capsys):
+    # the per-operation table comes from a second pass; the roofline line's rate comes
+    # from the dominant operation's own events over the timed region (passed as `dom`)
+    import argparse
+    import json
+
+    T, d, r, ffn, S, steps = 16384, 4096, 1024, 11008, 8, 10
+    args = argparse.Namespace(steps=steps, warmup=5, workload=bench.WORKLOAD, skip_aux=True,
+                              timing="eager", step_ms=None)
+    prof = {"gemm_dual": (2 * steps, 10.0, 7.6e12 * steps, 1e9),
+            "gemm_up_swiglu": (steps, 5.0, 1.5e12 * steps, 1e9)}
+    dom = ("gemm_dual", (2 * steps, 9.5, 7.6e12 * steps, 1e9))
+    assert bench._report(args, 1, prof, {}, {}, 36.0, float("nan"), 0, 0, T, d, r, ffn, S,
+                         dom=dom) == 0
+    roof = json.loads(capsys.readouterr().out.strip().splitlines()[-1])["roofline"]
+    assert roof["kernel"] == "gemm_dual"
+    assert roof["achieved"] == pytest.approx(7.6e12 * steps / 9.5e-3 / 1e12)
+    assert roof["launches_per_step"] == 2
