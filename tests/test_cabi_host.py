@@ -203,3 +203,10 @@ def test_bottleneck_up_projection_argument_checks(L):
                             f(0x100000), ws_bytes, None) == 3   # a misaligned
     assert L.boost_block_up(ctypes.byref(desc), f(0x1000), f(0x2000), f(0x3000), None,
                             f(0x100000), 64, None) == 4          # workspace too small
+
+
+def test_profile_only_argument_checks(L):
+    # one kernel id, or -1 for every kernel; anything else is rejected
+    n = L.boost_profile_kernel_count()
+    assert L.boost_profile_only(-2) == 1 and L.boost_profile_only(n) == 1
+    assert L.boost_profile_only(n - 1) == 0 and L.boost_profile_only(-1) == 0

@@ -199,6 +199,35 @@ def test_co_scheduled_gemms_count_two_kernels():
         assert kernels[name] == ops[name][0], name
 
 
+def test_profiling_one_kernel_alone():
+    # boost_profile_only restricts the timed operations to one kernel; the others run
+    # untimed, and every operation is timed again once the restriction is lifted
+    T, d, r, k, n, S = 512, 256, 128, 2, 512, 4
+    w = inputs.make_block(T, d, r, k, n, seed=14)
+    blk = Block(T, d, r, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    try:
+        B.profile_only("gemm_dual")
+        B.profile_enable(True)
+        blk.forward(x)
+        blk.backward(x, dy)
+        torch.cuda.synchronize()
+        ops = B.profile_read()
+        assert set(ops) == {"gemm_dual"} and ops["gemm_dual"][0] == 1
+        B.profile_only(None)
+        B.profile_enable(True)
+        blk.forward(x)
+        blk.backward(x, dy)
+        torch.cuda.synchronize()
+        ops = B.profile_read()
+        assert {"gemm_dual", "gemm_down_act", "gemm_up", "gemm_dx"} <= set(ops)
+    finally:
+        B.profile_only(None)
+        B.profile_enable(False)
+    with pytest.raises(KeyError):
+        B.profile_only("no_such_kernel")
+
+
 @pytest.mark.skipif(os.environ.get("BOOST_COSCHED_COLS", "") == "0",
                     reason="column co-scheduling turned off in the environment")
 def test_weight_gradient_columns_are_co_scheduled():
