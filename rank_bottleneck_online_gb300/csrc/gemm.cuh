@@ -65,6 +65,12 @@ constexpr int kEpiHalves = kEpiWarps / 4;
 #ifndef BOOST_GLU_IN_PLACE
 #define BOOST_GLU_IN_PLACE 1
 #endif
+// Dual recompute + dgrad: the bottleneck activation a = act(s z) is formed and stored as
+// soon as the first segment's MMAs (z) complete, while the second segment's still run;
+// only dzs and the row sums wait for the whole tile. 0: all of it after the whole tile.
+#ifndef BOOST_DUAL_SPLIT_EPI
+#define BOOST_DUAL_SPLIT_EPI 1
+#endif
 constexpr int kGluEpiWarps = BOOST_GLU_EPI_WARPS;
 
 enum EpiMode : int {
@@ -195,8 +201,10 @@ struct GemmCfg {
   static constexpr int kTmemColsRaw = kAccStages * kAccCols;
   static constexpr int kTmemCols = kTmemColsRaw <= 32 ? 32 : kTmemColsRaw <= 64 ? 64
                                    : kTmemColsRaw <= 128 ? 128 : kTmemColsRaw <= 256 ? 256 : 512;
+  // dual modes: one "z complete" barrier per accumulator set (the first segment's MMAs)
+  static constexpr int kZBars = (is_dual(MODE) && BOOST_DUAL_SPLIT_EPI) ? kAccStages : 0;
   static constexpr int kBarBytes =
-      8 * (2 * kStages + kAccStages + kTemptyBars + 1 + kLdBars) + 16;
+      8 * (2 * kStages + kAccStages + kTemptyBars + 1 + kLdBars + kZBars) + 16;
   // staging slots 1024-byte aligned (the 64-byte swizzle pattern of a TMA box repeats
   // every 512 bytes)
   static constexpr int kStgOffset = (kStages * kStageBytes + kBarBytes + 1023) / 1024 * 1024;
@@ -654,6 +662,39 @@ __device__ __forceinline__ void glu_chunk_in_place(const GemmParams& p, Loader& 
   ld.refill(lane);
 }
 
+// First part of the dual modes' epilogue, run while the tile's second segment is still
+// on the tensor cores: this warp's chunks of the bottleneck activation
+// a = bf16(act(s * z)) from the complete z accumulator (TMEM columns [0, BN) at t_row),
+// with the same expression as the forward's down-projection epilogue, so the
+// recomputed a is bitwise the forward's.
+template <int BN, int kHalves, int kSlots, bool kTma>
+__device__ __forceinline__ void dual_act_chunks(const GemmParams& p, int32_t row0, int32_t n0,
+                                                int32_t n_end, uint32_t t_row,
+                                                StoreRing<kSlots, kTma>& ring, int lane,
+                                                int half) {
+  const int32_t row = row0 + lane;
+  const int rows_valid = p.M - row0 < 32 ? p.M - row0 : 32;
+  const float s_row = (p.rstd != nullptr && row < p.M) ? p.rstd[row] : 1.0f;
+#pragma unroll 1
+  for (int c = half; c < BN / 32; c += kHalves) {
+    const int32_t col0 = n0 + c * 32;
+    const int cols_valid = n_end - col0;
+    if (cols_valid <= 0) break;            // warp-uniform
+    const bool whole = cols_valid >= 32 || n_end == p.N;
+    float v[32];
+    tmem_ld_32x32b_x32(t_row + c * 32, v);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(act_fwd(s_row * v[2 * i], p.act), act_fwd(s_row * v[2 * i + 1], p.act));
+    const int64_t base = static_cast<int64_t>(row0) * p.ldo + col0;
+    store_chunk_bf16(ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, 0,
+                     static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
+    if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
+  }
+}
+
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
@@ -740,7 +781,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
               if (i + h < cols_valid) rowsum += dz * z;
               d2[h] = s_row * dz;
             }
-            pk[i / 2] = pack_bf16x2(a2[0], a2[1]);
+            if constexpr (!BOOST_DUAL_SPLIT_EPI) pk[i / 2] = pack_bf16x2(a2[0], a2[1]);
             pk2[i / 2] = pack_bf16x2(d2[0], d2[1]);
           }
           __nv_bfloat16* o2 = static_cast<__nv_bfloat16*>(p.out2) +
@@ -798,11 +839,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(g_row * v[2 * i], g_row * v[2 * i + 1]);
         }
-        const int64_t base = tc.batch * p.out_bstride + static_cast<int64_t>(row0) * p.ldo + col0;
-        store_chunk_bf16<kSlots, kTma, MODE == EPI_GLU>(
-            ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
-            static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
-        if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
+        // (dual modes with the split epilogue stored a before the tile was complete)
+        if constexpr (!(is_dual(MODE) && BOOST_DUAL_SPLIT_EPI)) {
+          const int64_t base =
+              tc.batch * p.out_bstride + static_cast<int64_t>(row0) * p.ldo + col0;
+          store_chunk_bf16<kSlots, kTma, MODE == EPI_GLU>(
+              ring, lane, pk, &p.tmO[0], whole && (p.tma_out & 1), col0, row0, tc.batch,
+              static_cast<__nv_bfloat16*>(p.out) + base, p.ldo, rows_valid, cols_valid);
+          if (p.visits != nullptr) count_writes(p, base, lane, rows_valid, cols_valid);
+        }
       }
     }
   }
@@ -930,7 +975,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
   uint64_t* tempty_bar = tfull_bar + Cfg::kAccStages;
   uint64_t* done_bar = tempty_bar + Cfg::kTemptyBars;
   uint64_t* ld_bar = done_bar + 1;                   // kLdBars: the epilogue loaders'
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ld_bar + Cfg::kLdBars);
+  uint64_t* zfull_bar = ld_bar + Cfg::kLdBars;       // kZBars: z of the dual modes complete
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(zfull_bar + Cfg::kZBars);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -955,6 +1001,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
       mbar_init(&tempty_bar[s], Cfg::kEpiW * CG);   // one arrival per epilogue warp of the pair
     mbar_init(done_bar, 1);
     for (int s = 0; s < Cfg::kLdBars; ++s) mbar_init(&ld_bar[s], 1);
+    for (int s = 0; s < Cfg::kZBars; ++s) mbar_init(&zfull_bar[s], 1);
     fence_barrier_init();
   }
   if (warp == 2 && lane == 0 && Cfg::kEpiStreams > 0 && p.tma_in) {
@@ -1132,6 +1179,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
               phase ^= 1u;
             }
           }
+          if constexpr (Cfg::kZBars > 0) {
+            // dual modes: z (segment 0) is complete once these MMAs are; the epilogue
+            // stores a = act(s z) while segment 1 runs
+            if (sg == 0 && ok) {
+              if constexpr (CG == 2)
+                tc_commit_pair_mc(&zfull_bar[acc], static_cast<uint16_t>(0x3u << leader_rank));
+              else
+                tc_commit(&zfull_bar[acc]);
+            }
+          }
         }
         if constexpr (CG == 2)
           tc_commit_pair_mc(&tfull_bar[acc], static_cast<uint16_t>(0x3u << leader_rank));
@@ -1186,8 +1243,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
     uint32_t acc_phase = 0;
     for (int32_t tile = first_tile; tile < num_tiles; tile += tile_stride) {
       const TileCoord tc = decode_tile<Cfg::kTileN, Cfg::kTileM>(p, tile);
-      if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
-      tc_fence_after();
       const int32_t row0 = tc.m0 + static_cast<int32_t>(pm) * (kBM * CG) +
                            static_cast<int32_t>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -1195,6 +1250,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
       // this pair's columns of the super-tile (may be empty past the group or N end)
       const int32_t pn0 = tc.n0 + static_cast<int32_t>(pn) * BN;
       const int32_t pend = min(pn0 + BN, tc.n_end);
+      if constexpr (Cfg::kZBars > 0) {
+        if (!bounded_wait(&zfull_bar[acc], acc_phase, p.err, 11, p.wait_limit_ns)) break;
+        tc_fence_after();
+        dual_act_chunks<BN, Cfg::kHalves, Cfg::kStoreSlots, Cfg::kTmaStore>(
+            p, row0, pn0, pend, t_row, ring, lane, half);
+      }
+      if (!bounded_wait(&tfull_bar[acc], acc_phase, p.err, 4, p.wait_limit_ns)) break;
+      tc_fence_after();
       if constexpr (MODE == EPI_UPGLU) {
         epilogue_upglu<BN, CG, Cfg::kHalves, Cfg::kStoreSlots, Cfg::kTmaStore>(
             p, row0, pn0, pend, t_row, ring, lane, half,
