@@ -132,6 +132,8 @@ CASES = [
     ("co_scheduled_rows", 4352, 512, 512, 2, 1024, 4, "silu", True),
     # dB's 16 column super-tiles split between the cluster launch and a pair launch
     ("co_scheduled_cols", 1024, 256, 512, 2, 8192, 4, "silu", True),
+    # the down-projection and the dual kernel take the planned row split
+    ("planned_row_split", 9216, 1024, 512, 1, 2048, 4, "silu", True),
 ]
 
 

@@ -58,6 +58,9 @@ CASES = [
     ("no_norm_tail", 130, 128, 64, 1, 64, 2, False),
     ("co_scheduled_rows", 4352, 512, 512, 2, 1024, 4, True),
     ("co_scheduled_columns", 1024, 256, 512, 2, 8192, 4, True),
+    # the down-projection and the dual kernel take the planned row split (15 rows of
+    # 512-row super-tiles in the cluster launch instead of the fixed split's 16)
+    ("planned_row_split", 9216, 1024, 512, 1, 2048, 4, True),
 ]
 
 
