@@ -181,12 +181,21 @@ struct Plan {
 // where a wave is one pass of `groups` CTA groups over the tile list, t_kb is the
 // time of one 64-deep k-block of a 256x256 tile on a CTA pair (about 0.5 us at the
 // measured ~1.2-1.3 PFLOP/s), and the fp32 partials are written once and read once.
+int env_int(const char* name, int dflt);
+
 void choose_splits(int64_t tiles, int64_t nkb, int groups, int64_t out_elems, int& splits,
                    int& kbps) {
   constexpr double kTkb = 0.5e-6;          // seconds per k-block per tile
   constexpr double kHbm = 6.0e12;          // bytes per second
   splits = 1;
   kbps = static_cast<int>(nkb);
+  static const int forced = env_int("BOOST_SPLITK", 0);   // > 0: this many splits (tuning)
+  if (forced > 0) {
+    const int64_t per = cdiv(nkb, std::min<int64_t>(forced, 8));
+    splits = static_cast<int>(cdiv(nkb, per));
+    kbps = static_cast<int>(per);
+    return;
+  }
   double best = 1e300;
   for (int s = 1; s <= 8; ++s) {
     if (s > 1 && nkb / s < 4) break;
