@@ -39,3 +39,24 @@ def oracle_block(w, *, act, has_norm, S, eps=1e-5):
     y, c = oracle.block_fwd(x, g, A, Bw, act=act, has_norm=has_norm, eps=eps, S=S, flow="bf16")
     gr = oracle.block_bwd(x, g, A, Bw, dy, act=act, has_norm=has_norm, eps=eps, S=S, flow="bf16")
     return y, c, gr
+
+
+def random_block_shapes(count=16, seed=2026):
+    """Block shapes drawn once from a fixed seed within the library's shape rules (d, r,
+    n multiples of 8; S divides d when normed; k * r <= 1024, d <= 1024, n <= 2048,
+    T <= 5000, so the oracle takes seconds): any mix of ragged tails, group widths,
+    group counts, row splits and split-K plans the planner picks for them. Each is
+    (name, T, d, r, k, n, S, act, has_norm)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(count):
+        has_norm = bool(rng.integers(0, 4) > 0)
+        d = 8 * int(rng.integers(1, 129))
+        S = int(rng.choice([s for s in (1, 2, 4, 8) if d % s == 0])) if has_norm else 1
+        k = int(rng.integers(1, 5))
+        r = 8 * int(rng.integers(1, 1024 // (8 * k) + 1))
+        n = 8 * int(rng.integers(1, 257))
+        T = int(rng.integers(1, 5001))
+        act = "silu" if rng.integers(0, 5) > 0 else "identity"
+        out.append((f"rand{i}_T{T}_d{d}_r{r}_k{k}_n{n}", T, d, r, k, n, S, act, has_norm))
+    return out

@@ -19,7 +19,7 @@ from rank_bottleneck_online_gb300 import build as build_mod
 from rank_bottleneck_online_gb300 import inputs
 from rank_bottleneck_online_gb300.block import Block
 
-from parity import assert_close, oracle_block, to_np
+from parity import assert_close, oracle_block, random_block_shapes, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -411,3 +411,25 @@ def test_two_host_threads_on_their_own_streams_match_serial_runs():
         B.check(blk.ws)
         for a, b in zip(outputs(blk), want):
             assert torch.equal(a, b)
+
+
+# ------------------------------------------------------- seeded random shapes
+# (drawn once from a fixed seed within the shape rules: see parity.random_block_shapes)
+
+RANDOM_CASES = random_block_shapes()
+
+
+@pytest.mark.parametrize("case", RANDOM_CASES, ids=[c[0] for c in RANDOM_CASES])
+def test_seeded_random_shapes_parity(case):
+    name, T, d, r, k, n, S, act, has_norm = case
+    w, blk, a_fwd, a_bwd = _run_block(*case, seed=T)
+    y, c, gr = oracle_block(w, act=act, has_norm=has_norm, S=S)
+    assert_close("y", blk.y, y)
+    assert_close("a", a_fwd, c["a"])
+    assert torch.equal(a_fwd, a_bwd)
+    if has_norm:
+        np.testing.assert_allclose(to_np(blk.rstd), c["s"], rtol=2e-6)
+        assert_close("dgamma", blk.dgamma, gr["dgamma"])
+    assert_close("dx", blk.dx, gr["dx"])
+    assert_close("dA", blk.dA, gr["dA"])
+    assert_close("dB", blk.dB, gr["dB"])

@@ -17,6 +17,8 @@ from rank_bottleneck_online_gb300 import build as build_mod
 from rank_bottleneck_online_gb300 import inputs
 from rank_bottleneck_online_gb300.block import Block
 
+from parity import random_block_shapes
+
 pytestmark = pytest.mark.gpu
 
 GUARD = 4096          # bytes on each side; keeps the interior 256-byte aligned
@@ -62,6 +64,8 @@ CASES = [
     # 512-row super-tiles in the cluster launch instead of the fixed split's 16)
     ("planned_row_split", 9216, 1024, 512, 1, 2048, 4, True),
 ]
+# and the seeded random shapes of the block parity test
+CASES += [(c[0], *c[1:7], c[8]) for c in random_block_shapes()]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
