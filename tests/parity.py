@@ -60,3 +60,19 @@ def random_block_shapes(count=16, seed=2026):
         act = "silu" if rng.integers(0, 5) > 0 else "identity"
         out.append((f"rand{i}_T{T}_d{d}_r{r}_k{k}_n{n}", T, d, r, k, n, S, act, has_norm))
     return out
+
+
+def random_mlp_shapes(count=6, seed=2027):
+    """LLaMA-MLP shapes (T, d, r, ffn, S) drawn once from a fixed seed within the shape
+    rules (d, r, ffn multiples of 8, S divides d; T <= 4000, d <= 1024, r <= 512,
+    ffn <= 2048)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        d = 8 * int(rng.integers(1, 129))
+        S = int(rng.choice([s for s in (1, 2, 4, 8) if d % s == 0]))
+        r = 8 * int(rng.integers(1, 65))
+        ffn = 8 * int(rng.integers(1, 257))
+        T = int(rng.integers(1, 4001))
+        out.append((T, d, r, ffn, S))
+    return out
