@@ -710,7 +710,7 @@ def ours_arm(args):
                        T, c["d"], c["r"], c.get("ffn"), c["S"], dom=dom)
 
     aux = not args.skip_aux
-    e2e_s = _e2e(args, mlp, w, x, dout, T, d, dev) if aux else float("nan")
+    e2e_s, e2e_launch = _e2e(args, mlp, w, x, dout, T, d, dev) if aux else (float("nan"), None)
     btp = _btp_exchange(mlp, x, T, d, r, ffn, S) if aux else None
     dense = _dense_context(T, d, ffn, ms_total / args.steps) if aux else None
     cuts = (_checkpoint_cuts(mlp, w, x, dout, T, d, r, ffn, S, ms_total / args.steps)
@@ -718,7 +718,7 @@ def ours_arm(args):
     bi = 2 * T * d * 2          # x and dout, bf16
     bo = 2 * T * d * 2          # out and dx, bf16
     return _report(args, 1, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r,
-                   ffn, S, btp, dense, cuts, dom=dom)
+                   ffn, S, btp, dense, cuts, dom=dom, e2e_launch=e2e_launch)
 
 
 def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
@@ -773,11 +773,13 @@ def _btp_exchange(mlp, x, T, d, r, ffn, S, reps=5):
 
 
 def _e2e(args, mlp, w, x, dout, T, d, dev):
-    """Seconds for args.steps steps through the public API from pinned host buffers:
-    each step copies its x and dout in, runs forward + backward and copies out and dx
-    back. The copies are pipelined against the compute on two more streams (inputs of
-    step i+1 in, results of step i-1 out, while step i computes) with double-buffered
-    device tensors; every step's copies lie inside the timed region."""
+    """(seconds, launch) for args.steps steps through the public API from pinned host
+    buffers: each step copies its x and dout in, runs forward + backward and copies out
+    and dx back. The copies are pipelined against the compute on two more streams (inputs
+    of step i+1 in, results of step i-1 out, while step i computes) with double-buffered
+    device tensors; every step's copies lie inside the timed region. Like the timed
+    region, the K steps (copies included) are captured into one CUDA graph and launched
+    once unless --eager is given or the capture fails; `launch` says which ran."""
     import torch
 
     from rank_bottleneck_online_gb300.block import MLP
@@ -793,7 +795,6 @@ def _e2e(args, mlp, w, x, dout, T, d, dev):
     mlps = [mlp, MLP(T, d, r, ffn, S=S, weights=w, device=dev)]
     xs = [x, torch.empty_like(x)]
     douts = [dout, torch.empty_like(dout)]
-    comp = torch.cuda.current_stream()
     h2d = torch.cuda.Stream()
     d2h = torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()   # noqa: E731
@@ -801,16 +802,25 @@ def _e2e(args, mlp, w, x, dout, T, d, dev):
     computed = [ev(), ev()]
     copied_out = [ev(), ev()]
 
-    def run(n):
+    def run(n, capturing=False):
+        comp = torch.cuda.current_stream()
+        if capturing:
+            # the copy streams join the capture from the capturing stream; the first two
+            # steps' buffers are free (everything before the capture has completed)
+            h2d.wait_stream(comp)
+            d2h.wait_stream(comp)
         for i in range(n):
             b = i % 2
+            first = capturing and i < 2
             with torch.cuda.stream(h2d):
-                h2d.wait_event(computed[b])          # step i-2 finished with these inputs
+                if not first:
+                    h2d.wait_event(computed[b])      # step i-2 finished with these inputs
                 xs[b].copy_(x_h, non_blocking=True)
                 douts[b].copy_(dout_h, non_blocking=True)
                 in_ready[b].record(h2d)
             comp.wait_event(in_ready[b])
-            comp.wait_event(copied_out[b])            # step i-2's results are out
+            if not first:
+                comp.wait_event(copied_out[b])        # step i-2's results are out
             mlps[b].forward(xs[b])
             mlps[b].backward(xs[b], douts[b])
             computed[b].record(comp)
@@ -819,13 +829,29 @@ def _e2e(args, mlp, w, x, dout, T, d, dev):
                 out_h[b].copy_(mlps[b].out, non_blocking=True)
                 dx_h[b].copy_(mlps[b].gu.dx, non_blocking=True)
                 copied_out[b].record(d2h)
+        if capturing:
+            comp.wait_stream(h2d)
+            comp.wait_stream(d2h)
 
     run(2)
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                run(args.steps, capturing=True)
+        except Exception as ex:  # noqa: BLE001
+            print(f"end-to-end graph capture failed, running eagerly: {ex}", file=sys.stderr)
+            graph = None
+        torch.cuda.synchronize()
     t0 = time.perf_counter()
-    run(args.steps)
+    if graph is not None:
+        graph.replay()
+    else:
+        run(args.steps)
     torch.cuda.synchronize()
-    return time.perf_counter() - t0
+    return time.perf_counter() - t0, ("cuda_graph" if graph is not None else "eager")
 
 
 # Operations the library runs concurrently with other GEMMs (unless BOOST_FORK_STREAMS=0):
@@ -848,7 +874,7 @@ def dominant_kernel(prof, overlapped):
 
 
 def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T, d, r, ffn,
-            S, btp=None, dense=None, cuts=None, dom=None):
+            S, btp=None, dense=None, cuts=None, dom=None, e2e_launch=None):
     """The JSON line. `prof` / `prof_kernels`: every operation's events over K steps;
     `dom`: (name, (launches, ms, flops, bytes)) of the dominant operation timed alone over
     the timed region (None: taken from `prof`)."""
@@ -941,7 +967,8 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
         "gpu_launches": gpu_launches,
         "e2e": None if args.skip_aux or not default else {
             "value": aggregate_rate(world, T * args.steps, e2e_s), "unit": "tokens/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            **({"launch": e2e_launch} if e2e_launch else {})},
         "clocks": clocks,
         "cpu_baseline": cpu,
         "btp_exchange": btp,
