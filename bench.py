@@ -583,7 +583,12 @@ def _workload_step(name, wl, w, dev):
         dout = w["dout"].to(dev)
         return lambda: (wl.forward(x), wl.backward(x, dout))
     if kind == "layer":
-        dout, dq, dk = (w[k].to(dev) for k in ("dout", "dq", "dk"))
+        # dq and dk stand in for the (excluded) attention core's gradients: placed once in
+        # the stacked QKV gradient, where an attention backward would write them
+        dout = w["dout"].to(dev)
+        wl.dqkv[0].copy_(w["dq"])
+        wl.dqkv[1].copy_(w["dk"])
+        dq, dk = wl.dqkv[0], wl.dqkv[1]
         return lambda: (wl.forward(x), wl.backward(x, dout, dq, dk))
     dq, dg = w["dy_qkv"].to(dev), w["dy_gu"].to(dev)
     return lambda: (wl.forward(x), wl.backward(x, dq, dg))

@@ -143,6 +143,28 @@ boost_status boost_block_fwd_swiglu(const boost_block_desc* desc,
                                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Forward of one block with one output group (desc->k == 1) and a residual added
+ * in the up-projection's epilogue: y = res + block(x), for a transformer layer's
+ * residual connection around a block (the O projection, the MLP's down
+ * projection). The sum is formed as a separate add pass would form it: the block's
+ * output rounded to bf16, plus res, rounded to bf16. It is bitwise equal to
+ * boost_block_fwd followed by boost_add, without writing and reading the block's
+ * own output. The residual connection belongs to the LLaMA-2 layer (technical
+ * summary §4); the fusion is this library's.
+ *   x, gamma, A, B, rstd, ws  as in boost_block_fwd
+ *   res    [T, n]     the residual (device, bf16, 16-byte aligned; disjoint from y, or y
+ *                     itself); may be NULL only when T == 0
+ *   y      [1, T, n]  out: res + block(x)
+ * Errors: as boost_block_fwd, plus BOOST_ERR_INVALID_ARG for k != 1 or a NULL res,
+ * BOOST_ERR_ALIGNMENT for a misaligned res. The up-projection always uses its
+ * plain-store epilogue here (no TMA stores).
+ */
+boost_status boost_block_fwd_residual(const boost_block_desc* desc,
+                                      const void* x, const void* gamma, const void* A,
+                                      const void* B, const void* res, void* y, float* rstd,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Backward of one block with recompute (technical summary §2.2,
  * communication-free low-rank activation checkpointing: only x is kept; the
  * r-wide activation is regenerated inside the block).
@@ -165,6 +187,25 @@ boost_status boost_block_bwd(const boost_block_desc* desc,
                              const float* rstd, const void* dy,
                              void* dx, void* dgamma, void* dA, void* dB,
                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward of one block whose input gradient is added to a residual gradient in
+ * the dx epilogue: dx = res + (the block's input gradient). This is the gradient of x
+ * through a residual connection x + block(x), with res the gradient arriving by the
+ * skip path. Formed as a separate add pass would form it: dx rounded to bf16, plus
+ * res, rounded to bf16. It is bitwise equal to boost_block_bwd followed by boost_add.
+ *   x, gamma, A, B, rstd, dy, dgamma, dA, dB, ws  as in boost_block_bwd
+ *   res    [T, d]  the residual gradient (device, bf16, 16-byte aligned; disjoint from
+ *                  dx, or dx itself); may be NULL only when T == 0
+ *   dx     [T, d]  out: res + the block's input gradient
+ * Errors: as boost_block_bwd, plus BOOST_ERR_INVALID_ARG for a NULL res,
+ * BOOST_ERR_ALIGNMENT for a misaligned res.
+ */
+boost_status boost_block_bwd_residual(const boost_block_desc* desc,
+                                      const void* x, const void* gamma, const void* A,
+                                      const void* B, const float* rstd, const void* dy,
+                                      const void* res, void* dx, void* dgamma, void* dA,
+                                      void* dB, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Backward of the down bottleneck of a LLaMA MLP (no norm) whose input is

@@ -34,7 +34,7 @@ EXPORTS = (
     "boost_profile_read", "boost_rmsnorm_rstd_noalloc", "boost_block_bwd_swiglu",
     "boost_profile_read_kernels", "boost_block_fwd_swiglu", "boost_block_fwd_btp",
     "boost_block_up", "boost_debug_count_writes", "boost_debug_count_log",
-    "boost_profile_only",
+    "boost_profile_only", "boost_block_fwd_residual", "boost_block_bwd_residual",
 )
 
 
@@ -79,6 +79,9 @@ def lib():
     L.boost_debug_count_log.argtypes = [ctypes.POINTER(i64), i64]
     L.boost_debug_count_log.restype = i64
     L.boost_block_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.boost_block_fwd_residual.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.boost_block_bwd_residual.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           sz, vp]
     L.boost_rmsnorm_stats.argtypes = [dp, vp, vp, vp, vp]
     L.boost_block_layout.argtypes = [dp, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -218,8 +221,10 @@ def rmsnorm_rstd_noalloc(desc: Desc, x, rstd=None, stream=None):
     return rstd
 
 
-def block_fwd(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=None, stream=None):
-    """y [k,T,n] (and the row scale into ``rstd`` if given)."""
+def block_fwd(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=None, stream=None,
+              residual=None):
+    """y [k,T,n] (and the row scale into ``rstd`` if given). With ``residual`` [T,n]
+    (k == 1): y = residual + block(x), added in the up-projection's epilogue."""
     bf = torch.bfloat16
     _need(x, "x", bf, (desc.T, desc.d))
     _need(A, "A", bf, (desc.d, desc.k * desc.r))
@@ -231,6 +236,13 @@ def block_fwd(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=None, s
     _need(y, "y", bf, (desc.k, desc.T, desc.n))
     if rstd is not None:
         _need(rstd, "rstd", torch.float32, (desc.T,))
+    if residual is not None:
+        _need(residual, "residual", bf, (desc.T, desc.n))
+        _check(lib().boost_block_fwd_residual(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(A),
+                                              _ptr(B), _ptr(residual), _ptr(y), _ptr(rstd),
+                                              ws.ptr, ws.nbytes, _stream(stream)),
+               "boost_block_fwd_residual")
+        return y
     _check(lib().boost_block_fwd(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(A), _ptr(B),
                                  _ptr(y), _ptr(rstd), ws.ptr, ws.nbytes, _stream(stream)),
            "boost_block_fwd")
@@ -317,8 +329,9 @@ def block_fwd_btp(desc: Desc, x, gamma, A, B, ws: Workspace, *, y=None, rstd=Non
 
 
 def block_bwd(desc: Desc, x, gamma, A, B, dy, ws: Workspace, *, rstd=None, dx=None,
-              dgamma=None, dA=None, dB=None, stream=None):
-    """Returns (dx, dgamma or None, dA, dB)."""
+              dgamma=None, dA=None, dB=None, stream=None, dx_residual=None):
+    """Returns (dx, dgamma or None, dA, dB). With ``dx_residual`` [T,d]: dx =
+    dx_residual + the block's input gradient, added in the dx epilogue."""
     bf = torch.bfloat16
     _need(x, "x", bf, (desc.T, desc.d))
     _need(A, "A", bf, (desc.d, desc.k * desc.r))
@@ -337,6 +350,14 @@ def block_bwd(desc: Desc, x, gamma, A, B, dy, ws: Workspace, *, rstd=None, dx=No
             dgamma = torch.empty(desc.d, dtype=bf, device=dev)
     if rstd is not None:
         _need(rstd, "rstd", torch.float32, (desc.T,))
+    if dx_residual is not None:
+        _need(dx_residual, "dx_residual", bf, (desc.T, desc.d))
+        _check(lib().boost_block_bwd_residual(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(A),
+                                              _ptr(B), _ptr(rstd), _ptr(dy), _ptr(dx_residual),
+                                              _ptr(dx), _ptr(dgamma), _ptr(dA), _ptr(dB),
+                                              ws.ptr, ws.nbytes, _stream(stream)),
+               "boost_block_bwd_residual")
+        return dx, dgamma, dA, dB
     _check(lib().boost_block_bwd(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(A), _ptr(B),
                                  _ptr(rstd), _ptr(dy), _ptr(dx), _ptr(dgamma), _ptr(dA),
                                  _ptr(dB), ws.ptr, ws.nbytes, _stream(stream)),

@@ -40,14 +40,19 @@ class Block:
         self.dB = torch.empty(k, r, n, dtype=bf, device=self.device)
         self.dgamma = torch.empty(d, dtype=bf, device=self.device) if has_norm else None
 
-    def forward(self, x, stream=None):
+    def forward(self, x, stream=None, residual=None):
+        """residual [T, n] (k == 1): y = residual + block(x), added in the epilogue."""
         return B.block_fwd(self.desc, x, self.gamma, self.A, self.B, self.ws, y=self.y,
-                           rstd=self.rstd, stream=stream)
+                           rstd=self.rstd, stream=stream, residual=residual)
 
-    def backward(self, x, dy, stream=None, reuse_rstd=True):
+    def backward(self, x, dy, stream=None, reuse_rstd=True, dx=None, dx_residual=None):
+        """dx: where the input gradient goes (default: this block's own buffer);
+        dx_residual [T, d]: added to it in the dx epilogue."""
         return B.block_bwd(self.desc, x, self.gamma, self.A, self.B, dy, self.ws,
-                           rstd=self.rstd if reuse_rstd else None, dx=self.dx,
-                           dgamma=self.dgamma, dA=self.dA, dB=self.dB, stream=stream)
+                           rstd=self.rstd if reuse_rstd else None,
+                           dx=self.dx if dx is None else dx,
+                           dgamma=self.dgamma, dA=self.dA, dB=self.dB, stream=stream,
+                           dx_residual=dx_residual)
 
 
 class MLP:
@@ -88,7 +93,8 @@ class MLP:
     def out(self):
         return self.dn.y[0]
 
-    def forward(self, x, stream=None):
+    def forward(self, x, stream=None, residual=None):
+        """residual [T, d]: out = residual + MLP(x), added in the down block's epilogue."""
         if self.fused_glu:
             gu = self.gu
             B.block_fwd_swiglu(gu.desc, x, gu.gamma, gu.A, gu.B, gu.ws, y=gu.y, h=self.h,
@@ -96,7 +102,7 @@ class MLP:
         else:
             y1 = self.gu.forward(x, stream)
             B.swiglu_fwd(y1[0], y1[1], self.h, stream=stream)
-        return self.dn.forward(self.h, stream)[0]
+        return self.dn.forward(self.h, stream, residual=residual)[0]
 
     def saved_bytes(self):
         """Bytes of activations the backward needs from the forward beyond the input x
@@ -106,7 +112,8 @@ class MLP:
             return 3 * self.T * self.ffn * 2
         return self.T * 2 * self.r * 2
 
-    def backward(self, x, dout, stream=None):
+    def backward(self, x, dout, stream=None, dx_residual=None):
+        """dx_residual [T, d]: added to the MLP's input gradient in the dx epilogue."""
         dy2 = dout.view(1, self.T, self.d)
         if self.checkpoint == "bottleneck":
             gu = self.gu
@@ -121,7 +128,7 @@ class MLP:
             dh = self.dn.backward(self.h, dy2, stream)[0]
             B.swiglu_bwd(self.gu.y[0], self.gu.y[1], dh, self.dy1[0], self.dy1[1],
                          stream=stream)
-        return self.gu.backward(x, self.dy1, stream)
+        return self.gu.backward(x, self.dy1, stream, dx_residual=dx_residual)
 
     def grads(self):
         return {"dx": self.gu.dx, "dgamma": self.gu.dgamma, "dA1": self.gu.dA, "dB1": self.gu.dB,
@@ -129,7 +136,12 @@ class MLP:
 
 
 class Layer:
-    """QKV (normed, k=3) -> O (k=1) on V -> residual -> MLP -> residual."""
+    """QKV (normed, k=3) -> O (k=1) on V -> residual -> MLP -> residual.
+
+    Both residual adds run in GEMM epilogues: x1 = x + O(v) in the O block's
+    up-projection, out = x1 + MLP(x1) in the MLP's down up-projection; in the backward,
+    dx1 = dout + (MLP input gradient) in the MLP's dx epilogue and dx = dx1 + (QKV input
+    gradient) in the QKV block's."""
 
     def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, act="silu", weights=None, device="cuda"):
         p = weights or {}
@@ -147,29 +159,46 @@ class Layer:
         for blk in (self.qkv, self.o):
             blk.ws = ws
         dev = self.qkv.device
-        bf = torch.bfloat16
-        self.x1 = torch.empty(T, d, dtype=bf, device=dev)
-        self.out = torch.empty(T, d, dtype=bf, device=dev)
-        self.dx1 = torch.empty(T, d, dtype=bf, device=dev)
-        self.dqkv = torch.empty(3, T, d, dtype=bf, device=dev)
-        self.dx = torch.empty(T, d, dtype=bf, device=dev)
+        self.dqkv = torch.empty(3, T, d, dtype=torch.bfloat16, device=dev)
+
+    @property
+    def x1(self):
+        """x + O(v): the MLP's input (the O block's output buffer)."""
+        return self.o.y[0]
+
+    @property
+    def out(self):
+        """x1 + MLP(x1) (the MLP's output buffer)."""
+        return self.mlp.out
+
+    @property
+    def dx1(self):
+        """Gradient at x1: dout + the MLP's input gradient (the MLP's dx buffer)."""
+        return self.mlp.gu.dx
+
+    @property
+    def dx(self):
+        """Gradient at x: dx1 + the QKV block's input gradient (its dx buffer)."""
+        return self.qkv.dx
 
     def forward(self, x, stream=None):
         qkv = self.qkv.forward(x, stream)
-        o = self.o.forward(qkv[2], stream)[0]
-        B.add(x, o, self.x1, stream=stream)
-        m = self.mlp.forward(self.x1, stream)
-        return B.add(self.x1, m, self.out, stream=stream)
+        x1 = self.o.forward(qkv[2], stream, residual=x)[0]
+        return self.mlp.forward(x1, stream, residual=x1)
 
     def backward(self, x, dout, dq, dk, stream=None):
-        dxm = self.mlp.backward(self.x1, dout, stream)[0]
-        B.add(dout, dxm, self.dx1, stream=stream)
-        self.dqkv[0].copy_(dq)
-        self.dqkv[1].copy_(dk)
-        self.o.backward(self.qkv.y[2], self.dx1.view(1, self.T, self.d), stream)
-        self.dqkv[2].copy_(self.o.dx)
-        dxq = self.qkv.backward(x, self.dqkv, stream)[0]
-        return B.add(self.dx1, dxq, self.dx, stream=stream)
+        """dq, dk: the attention core's gradients of q and k. The QKV block's upstream
+        gradient is the stacked [dq, dk, dv]; dq and dk are copied into it unless they
+        are already its first two planes (`dqkv[0]`, `dqkv[1]`), and the O block writes
+        dv straight into the third."""
+        dx1 = self.mlp.backward(self.x1, dout, stream, dx_residual=dout)[0]
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            for i, g in enumerate((dq, dk)):
+                if g.data_ptr() != self.dqkv[i].data_ptr():
+                    self.dqkv[i].copy_(g)
+        self.o.backward(self.qkv.y[2], dx1.view(1, self.T, self.d), stream, dx=self.dqkv[2])
+        return self.qkv.backward(x, self.dqkv, stream, dx_residual=dx1)[0]
 
 
 class SVDPair:

@@ -717,9 +717,10 @@ boost_status boost_rmsnorm_stats(const boost_block_desc* desc, const void* x, fl
 namespace {
 
 // K3, the batched up-projection y[i] = a[:, group i] @ B[i]; with `glu` (k == 2) one
-// kernel computes both groups of a tile and also writes h = silu(y[0]) * y[1].
+// kernel computes both groups of a tile and also writes h = silu(y[0]) * y[1]. With
+// `res` (k == 1) the epilogue adds the residual: y = bf16(bf16(a @ B) + res).
 cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void* h, bool glu,
-                      DeviceError* err, int sms, cudaStream_t s) {
+                      DeviceError* err, int sms, cudaStream_t s, const void* res = nullptr) {
   cudaError_t e;
   GemmParams u = base_params(P, err);
   if (!make_map(&u.tmA[0], a, P.r, P.k, P.T, P.r * 2, P.kr * 2, 64, 1, P.up.a_rows()))
@@ -763,11 +764,14 @@ cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void
     e = launch_gemm_rows(P.up, EPI_UPGLU, u, sms, s);
   } else {
     // with a short K the epilogue's stores weigh most: store them through TMA
+    // (the residual is read by the plain-store epilogue)
     static const int tma_up_max_r = env_int("BOOST_TMA_UP_MAX_R", 512);
-    const bool tma = P.r <= tma_up_max_r;
+    const bool tma = P.r <= tma_up_max_r && res == nullptr;
     if (tma) set_out_maps(u, P.T, P.n, P.k);
+    u.res = static_cast<const __nv_bfloat16*>(res);
+    u.ldr = P.n;
     ProfScope ps(s, K_UP, 2.0 * P.T * P.kr * P.n,
-                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n));
+                 2.0 * (P.T * P.kr + P.kr * P.n + P.k * P.T * P.n * (res ? 2 : 1)));
     e = launch_gemm_rows(P.up, tma ? EPI_BF16T : EPI_BF16, u, sms, s);
   }
   return e;
@@ -781,12 +785,17 @@ cudaError_t launch_up(const Plan& P, const void* a, const void* B, void* y, void
 boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const void* gamma,
                             const void* A, const void* B, void* y, void* h, bool glu,
                             float* rstd, float* payload, bool btp, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            void* stream, const void* res = nullptr, bool with_res = false) {
   boost_status st = validate_desc(desc);
   if (st != BOOST_OK) return st;
   const boost_block_desc& D = *desc;
   if (!D.has_norm && (gamma != nullptr || rstd != nullptr)) return BOOST_ERR_INVALID_ARG;
   if (glu && D.k != 2) return BOOST_ERR_INVALID_ARG;
+  if (with_res) {
+    // y = res + block(x): one output group, res shaped like it
+    if (D.k != 1 || (D.T > 0 && res == nullptr)) return BOOST_ERR_INVALID_ARG;
+    if (res != nullptr && !aligned16(res)) return BOOST_ERR_ALIGNMENT;
+  }
   // With no tokens the [T, ...] tensors are empty and may be NULL.
   st = D.T == 0 ? check_ptrs({A, B}, {gamma, rstd, x, y, h})
                 : check_ptrs({x, A, B, y}, {gamma, rstd, h});
@@ -869,8 +878,8 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
   }
   if (e != cudaSuccess) return BOOST_ERR_CUDA;
 
-  // K3: y[i] = a[:, group i] @ B[i], batched over the k groups.
-  e = launch_up(P, a, B, y, h, glu, err, sms, s);
+  // K3: y[i] = a[:, group i] @ B[i], batched over the k groups (plus the residual).
+  e = launch_up(P, a, B, y, h, glu, err, sms, s, with_res ? res : nullptr);
   return cuda_status(e);
 }
 
@@ -919,6 +928,14 @@ boost_status boost_block_fwd_swiglu(const boost_block_desc* desc, const void* x,
                         stream);
 }
 
+boost_status boost_block_fwd_residual(const boost_block_desc* desc, const void* x,
+                                      const void* gamma, const void* A, const void* B,
+                                      const void* res, void* y, float* rstd, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  return block_fwd_impl(desc, x, gamma, A, B, y, nullptr, false, rstd, nullptr, false, ws,
+                        ws_bytes, stream, res, true);
+}
+
 }  // extern "C"
 
 namespace {
@@ -929,10 +946,15 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
                             const void* A, const void* B, const float* rstd, const void* dy,
                             void* dx, void* dgamma, void* dA, void* dB, const void* gate,
                             const void* up, void* dgate, void* dup, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            void* stream, const void* dx_res = nullptr, bool with_res = false) {
   boost_status st = validate_desc(desc);
   if (st != BOOST_OK) return st;
   const boost_block_desc& D = *desc;
+  if (with_res) {
+    // dx = res + the block's input gradient (res shaped like dx)
+    if (gate != nullptr || (D.T > 0 && dx_res == nullptr)) return BOOST_ERR_INVALID_ARG;
+    if (dx_res != nullptr && !aligned16(dx_res)) return BOOST_ERR_ALIGNMENT;
+  }
   const bool glu = gate != nullptr;
   if (!D.has_norm && (gamma != nullptr || rstd != nullptr || dgamma != nullptr))
     return BOOST_ERR_INVALID_ARG;
@@ -1130,6 +1152,10 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
     w.m_inner = 0;
     w.out = dx;
     w.ldo = P.d;
+    if (with_res) {
+      w.res = static_cast<const __nv_bfloat16*>(dx_res);
+      w.ldr = P.d;
+    }
     if (glu) {
       w.out = dgate;
       w.out2 = dup;
@@ -1153,7 +1179,8 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
       w.tma_in = 1;
     }
     ProfScope ps(s, glu ? K_DX_GLU : K_DX, 2.0 * P.T * P.kr * P.d,
-                 2.0 * (P.T * P.kr + P.d * P.kr + P.T * P.d * (glu ? 4 : (D.has_norm ? 2 : 1))) +
+                 2.0 * (P.T * P.kr + P.d * P.kr +
+                        P.T * P.d * (glu ? 4 : (D.has_norm ? 2 : 1) + (with_res ? 1 : 0))) +
                      4.0 * P.T * (P.n_cols_dual + 1));
     e = launch_gemm_rows(P.dx, glu ? EPI_GLU : EPI_DX, w, sms, s);
   }
@@ -1170,6 +1197,15 @@ boost_status boost_block_bwd(const boost_block_desc* desc, const void* x, const 
                              size_t ws_bytes, void* stream) {
   return block_bwd_impl(desc, x, gamma, A, B, rstd, dy, dx, dgamma, dA, dB, nullptr, nullptr,
                         nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+boost_status boost_block_bwd_residual(const boost_block_desc* desc, const void* x,
+                                      const void* gamma, const void* A, const void* B,
+                                      const float* rstd, const void* dy, const void* res,
+                                      void* dx, void* dgamma, void* dA, void* dB, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  return block_bwd_impl(desc, x, gamma, A, B, rstd, dy, dx, dgamma, dA, dB, nullptr, nullptr,
+                        nullptr, nullptr, ws, ws_bytes, stream, res, true);
 }
 
 boost_status boost_block_bwd_swiglu(const boost_block_desc* desc, const void* h, const void* A,

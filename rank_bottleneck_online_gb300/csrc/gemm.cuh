@@ -145,6 +145,9 @@ struct GemmParams {
   float* dgpart;              // EPI_DA out: [n_tiles][M]
   const __nv_bfloat16* gamma; // EPI_DA: gamma [M]
   const __nv_bfloat16* wA;    // EPI_DA: A [M, N]
+  const __nv_bfloat16* res;   // EPI_BF16, EPI_DX (one batch): residual [M, N] added to the
+                              // bf16 output, out = bf16(bf16(result) + res), or NULL
+  int64_t ldr;                // leading dimension of res
   DeviceError* err;
   uint64_t wait_limit_ns;
   int32_t* visits;            // debug: per-element write counts, indexed like out (or NULL)
@@ -695,6 +698,22 @@ __device__ __forceinline__ void dual_act_chunks(const GemmParams& p, int32_t row
   }
 }
 
+// out = bf16(bf16(result) + res) on this warp's packed 32 x 32 chunk, when the launch has a
+// residual: the same two roundings as storing the result and adding res in a separate
+// pass. The residual chunk comes in through the warp's 2 KB store block (coalesced rows),
+// which the chunk's store reuses afterwards.
+__device__ __forceinline__ void add_residual(const GemmParams& p, uint8_t* blk, int lane,
+                                             int32_t row0, int32_t col0, int rows_valid,
+                                             int cols_valid, uint32_t (&pk)[16]) {
+  if (p.res == nullptr) return;
+  float rv[32];
+  stage_load_bf16(blk, lane, p.res + static_cast<int64_t>(row0) * p.ldr + col0, p.ldr,
+                  rows_valid, cols_valid, rv);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    pk[i] = pack_bf16x2(bf16_lo(pk[i]) + rv[2 * i], bf16_hi(pk[i]) + rv[2 * i + 1]);
+}
+
 // Epilogue of one tile for the calling warp: its 32 TMEM lanes of the accumulator set
 // at column `t_row` hold output rows [row0, row0 + 32); this thread owns row0 + lane.
 // Columns [n0, n_end) are written, 32 at a time, through the warp's staging block.
@@ -760,6 +779,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         } else if constexpr (MODE == EPI_BF16 || MODE == EPI_BF16T) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          if constexpr (MODE == EPI_BF16) add_residual(p, ring.base, lane, row0, col0, rows_valid,
+                                                      cols_valid, pk);
         } else if constexpr (is_dual(MODE)) {
           // a = act(z) (recompute) and dzs = s * act'(z) * (dy B^T); row partial of dz * z.
           uint32_t pk2[16];
@@ -827,6 +848,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(v[2 * i] - coef * xv[0][2 * i],
                                 v[2 * i + 1] - coef * xv[0][2 * i + 1]);
+          add_residual(p, ring.base, lane, row0, col0, rows_valid, cols_valid, pk);
         } else if constexpr (MODE == EPI_DA) {
           if (p.wA != nullptr) {
             float av[32];

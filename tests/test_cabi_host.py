@@ -210,3 +210,33 @@ def test_profile_only_argument_checks(L):
     n = L.boost_profile_kernel_count()
     assert L.boost_profile_only(-2) == 1 and L.boost_profile_only(n) == 1
     assert L.boost_profile_only(n - 1) == 0 and L.boost_profile_only(-1) == 0
+
+
+def test_residual_entry_point_argument_checks(L):
+    # the residual forms of forward and backward reject, before enqueuing anything: more
+    # than one output group, a missing residual, a misaligned residual; the forward with
+    # T = 0 is a no-op (the backward's zeroed weight gradients need the device)
+    f = _fake
+    ok = B.make_desc(128, 256, 64, 1, 256, S=4)
+    ws_bytes = B.workspace_bytes(ok)
+
+    def fwd(desc, res, wsb=ws_bytes):
+        return L.boost_block_fwd_residual(ctypes.byref(desc), f(0x10000), f(0x20000),
+                                          f(0x30000), f(0x40000), f(res) if res else None,
+                                          f(0x50000), None, f(0x100000), wsb, None)
+
+    def bwd(desc, res, wsb=ws_bytes):
+        return L.boost_block_bwd_residual(ctypes.byref(desc), f(0x1000), f(0x2000), f(0x3000),
+                                          f(0x4000), None, f(0x5000), f(res) if res else None,
+                                          f(0x6000), f(0x6100), f(0x7000), f(0x8000),
+                                          f(0x100000), wsb, None)
+
+    three = B.make_desc(128, 256, 64, 3, 256, S=4)
+    assert fwd(three, 0x60000, B.workspace_bytes(three)) == 1   # k != 1
+    assert fwd(ok, 0) == 1                                      # no residual
+    assert fwd(ok, 0x60008) == 3                                # misaligned residual
+    assert bwd(ok, 0) == 1
+    assert bwd(ok, 0x60008) == 3
+    empty = B.make_desc(0, 256, 64, 1, 256, S=4)
+    wsb0 = B.workspace_bytes(empty) or 1 << 20
+    assert fwd(empty, 0, wsb0) == 0

@@ -91,6 +91,14 @@ def test_no_write_outside_any_output(case):
         pay = Guarded((B.btp_payload_elems(desc),), f32)
         B.block_fwd_btp(desc, x, gamma, A, Bw, ws, y=outs["y"].t, payload=pay.t)
         outs["payload"] = pay
+    if k == 1:
+        # the residual forms write the same outputs (plain-store epilogues)
+        res_y = torch.randn(T, n, device="cuda").to(bf)
+        res_x = torch.randn(T, d, device="cuda").to(bf)
+        B.block_fwd(desc, x, gamma, A, Bw, ws, y=outs["y"].t, rstd=rstd, residual=res_y)
+        B.block_bwd(desc, x, gamma, A, Bw, dy, ws, rstd=rstd, dx=outs["dx"].t,
+                    dgamma=outs["dgamma"].t if norm else None, dA=outs["dA"].t,
+                    dB=outs["dB"].t, dx_residual=res_x)
     if k == 2:
         h = Guarded((T, n), bf)
         B.block_fwd_swiglu(desc, x, gamma, A, Bw, ws, y=outs["y"].t, h=h.t, rstd=rstd)

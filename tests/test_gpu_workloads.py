@@ -66,6 +66,34 @@ def test_fused_swiglu_backward_matches_separate_passes(T, d, r, ffn):
         assert_close(k, g_f[k], g_s[k].double().cpu().numpy(), 1e-2, 1e-3)
 
 
+@pytest.mark.parametrize("T,d,r,n,norm", [(300, 128, 64, 200, False), (1000, 256, 640, 384, True),
+                                          (4352, 256, 128, 1024, True), (600, 264, 512, 520, False)])
+def test_fused_residual_matches_separate_add(T, d, r, n, norm):
+    # the layer's residual adds in GEMM epilogues: y = res + block(x) in the up-projection
+    # and dx = res + the block's dx in the dx epilogue, bit for bit what a separate add
+    # pass gives (same two bf16 roundings); the weight gradients are unchanged. Shapes:
+    # short r (whose up-projection otherwise stores through TMA), long r, co-scheduled
+    # rows, ragged last column tiles, normed and not.
+    S = 4 if norm else 1
+    w = inputs.make_block(T, d, r, 1, n, has_norm=norm, seed=8)
+    blk = Block(T, d, r, 1, n, S=S, has_norm=norm, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    g = torch.Generator().manual_seed(T)
+    res_y = torch.randn(T, n, generator=g).to(torch.bfloat16).cuda()
+    res_x = torch.randn(T, d, generator=g).to(torch.bfloat16).cuda()
+    y_sep = B.add(res_y, blk.forward(x)[0].clone())
+    grads_sep = [t.clone() if t is not None else None for t in blk.backward(x, dy)]
+    dx_sep = B.add(res_x, grads_sep[0])
+    y_f = blk.forward(x, residual=res_y)[0].clone()
+    grads_f = [t.clone() if t is not None else None for t in
+               blk.backward(x, dy, dx_residual=res_x)]
+    B.check(blk.ws)
+    assert torch.equal(y_f, y_sep)
+    assert torch.equal(grads_f[0], dx_sep)
+    for a, b in zip(grads_f[1:], grads_sep[1:]):
+        assert (a is None and b is None) or torch.equal(a, b)
+
+
 @pytest.mark.parametrize("T,d,r,n", [(512, 256, 128, 512), (600, 128, 64, 520), (300, 128, 64, 200),
                                      (4352, 256, 128, 1024), (6000, 256, 128, 1040)])
 def test_fused_swiglu_forward_matches_separate_passes(T, d, r, n):
@@ -274,13 +302,16 @@ def _sample_rows(T, n=192, seed=0):
     return np.sort(idx)
 
 
-def _full_T_block(tag, X, gamma, A, Bw, dy, got, *, S, act="silu"):
+def _full_T_block(tag, X, gamma, A, Bw, dy, got, *, S, act="silu", dx_residual=None):
     """One block's backward at full T against the oracle run on the inputs that block
     received on the GPU (X its input, dy its upstream gradient, both bf16 on the host):
-    every weight gradient (they sum over all T rows) and, where the GPU has it, dx."""
+    every weight gradient (they sum over all T rows) and, where the GPU has it, dx (plus
+    `dx_residual`, the skip path's gradient the GPU added in its dx epilogue)."""
     has_norm = gamma is not None
     g = oracle.block_bwd(inputs.as_f64(X), gamma, A, Bw, inputs.as_f64(dy), act=act,
                          has_norm=has_norm, S=S if has_norm else 1)
+    if dx_residual is not None:
+        g["dx"] = g["dx"] + inputs.as_f64(dx_residual)
     for k, v in got.items():
         assert_close(f"{tag} {k}", v, g[k])
     return g
@@ -303,16 +334,19 @@ def test_llama2_13b_layer_full_size():
     out = _f(L.forward(x))[idx]
     cpu = lambda t: t.detach().cpu()   # noqa: E731  (bf16 on the host)
     qkv_f, x1_f, gu_f, h_f = cpu(L.qkv.y), cpu(L.x1), cpu(L.mlp.gu.y), cpu(L.mlp.h)
-    qkv, o, x1 = _f(qkv_f)[:, idx], _f(L.o.y)[0][idx], _f(x1_f)[idx]
-    gu, h, dn = _f(gu_f)[:, idx], _f(h_f)[idx], _f(L.mlp.dn.y)[0][idx]
+    # (the residual adds run in the O and down blocks' epilogues: x1 and out are their
+    # outputs, and the MLP's and QKV block's dx epilogues add dout and dx1)
+    qkv, x1 = _f(qkv_f)[:, idx], _f(x1_f)[idx]
+    gu, h = _f(gu_f)[:, idx], _f(h_f)[idx]
     L.backward(x, w["dout"].cuda(), w["dq"].cuda(), w["dk"].cuda())
     B.check(L.qkv.ws)
     dy1_f, dx1_f, dqkv_f = cpu(L.mlp.dy1), cpu(L.dx1), cpu(L.dqkv)
-    dy1, dxm, dx1 = _f(dy1_f)[:, idx], _f(L.mlp.gu.dx)[idx], _f(dx1_f)[idx]
-    dv, dqkv, dxq, dx = _f(L.o.dx)[idx], _f(dqkv_f)[:, idx], _f(L.qkv.dx)[idx], _f(L.dx)[idx]
+    dy1, dx1 = _f(dy1_f)[:, idx], _f(dx1_f)[idx]
+    # the O block writes dv straight into the stacked QKV gradient's third plane
+    dv, dqkv, dx = _f(dqkv_f[2])[idx], _f(dqkv_f)[:, idx], _f(L.dx)[idx]
     wgrads = {"qkv": {"dA": cpu(L.qkv.dA), "dB": cpu(L.qkv.dB), "dgamma": cpu(L.qkv.dgamma),
                       "dx": cpu(L.qkv.dx)},
-              "o": {"dA": cpu(L.o.dA), "dB": cpu(L.o.dB), "dx": cpu(L.o.dx)},
+              "o": {"dA": cpu(L.o.dA), "dB": cpu(L.o.dB), "dx": dqkv_f[2]},
               "gu": {"dA": cpu(L.mlp.gu.dA), "dB": cpu(L.mlp.gu.dB),
                      "dgamma": cpu(L.mlp.gu.dgamma), "dx": cpu(L.mlp.gu.dx)},
               "dn": {"dA": cpu(L.mlp.dn.dA), "dB": cpu(L.mlp.dn.dB)}}
@@ -324,33 +358,30 @@ def test_llama2_13b_layer_full_size():
     yq, _ = oracle.block_fwd(X, p["gamma1"], p["A_qkv"], p["B_qkv"], S=S)
     assert_close("qkv", qkv, yq)
     yo, _ = oracle.block_fwd(qkv[2], None, p["A_o"], p["B_o"], has_norm=False)
-    assert_close("o", o, yo[0])
-    assert_close("x1", x1, X + o)
+    assert_close("x1", x1, X + ob.to_bf16(yo[0]))
     yg, _ = oracle.block_fwd(x1, p["gamma2"], p["A_gu"], p["B_gu"], S=S)
     assert_close("gate/up", gu, yg)
     assert_close("h", h, oracle.swiglu_fwd(gu[0], gu[1]))
     yd, _ = oracle.block_fwd(h, None, p["A_dn"], p["B_dn"], has_norm=False)
-    assert_close("down", dn, yd[0])
-    assert_close("out", out, x1 + dn)
+    assert_close("out", out, x1 + ob.to_bf16(yd[0]))
     gd = oracle.block_bwd(h, None, p["A_dn"], p["B_dn"], dout[None], has_norm=False)
     dg, du = oracle.swiglu_bwd(gu[0], gu[1], ob.to_bf16(gd["dx"]))
     assert_close("dgate", dy1[0], dg)
     assert_close("dup", dy1[1], du)
     gg = oracle.block_bwd(x1, p["gamma2"], p["A_gu"], p["B_gu"], dy1, S=S)
-    assert_close("dx mlp", dxm, gg["dx"])
-    assert_close("dx1", dx1, dout + dxm)
+    assert_close("dx1", dx1, dout + ob.to_bf16(gg["dx"]))
     go = oracle.block_bwd(qkv[2], None, p["A_o"], p["B_o"], dx1[None], has_norm=False)
     assert_close("dv", dv, go["dx"])
     gq = oracle.block_bwd(X, p["gamma1"], p["A_qkv"], p["B_qkv"], dqkv, S=S)
-    assert_close("dx qkv", dxq, gq["dx"])
-    assert_close("dx", dx, dx1 + dxq)
+    assert_close("dx", dx, dx1 + ob.to_bf16(gq["dx"]))
     # full T, one block at a time (host memory stays at one block's fp64 tensors)
     del yq, yo, yg, yd, gd, gg, go, gq
     _full_T_block("down", h_f, None, p["A_dn"], p["B_dn"], w["dout"][None], wgrads["dn"], S=S)
-    _full_T_block("gate/up", x1_f, p["gamma2"], p["A_gu"], p["B_gu"], dy1_f, wgrads["gu"], S=S)
+    _full_T_block("gate/up", x1_f, p["gamma2"], p["A_gu"], p["B_gu"], dy1_f, wgrads["gu"], S=S,
+                  dx_residual=w["dout"])
     _full_T_block("o", qkv_f[2], None, p["A_o"], p["B_o"], dx1_f[None], wgrads["o"], S=S)
     _full_T_block("qkv", w["x"], p["gamma1"], p["A_qkv"], p["B_qkv"], dqkv_f, wgrads["qkv"],
-                  S=S)
+                  S=S, dx_residual=dx1_f)
 
 
 @pytest.mark.slow
