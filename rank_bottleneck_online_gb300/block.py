@@ -202,7 +202,9 @@ class Layer:
 
 
 class SVDPair:
-    """Two normed SVD-style bottlenecks (identity act) on one x: QKV and gate/up."""
+    """Two normed SVD-style bottlenecks (identity act) on one x: QKV and gate/up. The
+    input gradient is the sum of the two blocks', added in the gate/up block's dx
+    epilogue."""
 
     def __init__(self, T, d, r, ffn, *, S=1, eps=1e-5, weights=None, device="cuda"):
         p = weights or {}
@@ -213,15 +215,18 @@ class SVDPair:
                         weights={"gamma": p.get("gamma_gu"), "A": p.get("A_gu"),
                                  "B": p.get("B_gu")}, device=device, ws=self.qkv.ws)
         self.qkv.ws = self.gu.ws
-        self.dx = torch.empty(T, d, dtype=torch.bfloat16, device=self.qkv.device)
+
+    @property
+    def dx(self):
+        """Gradient at x: the QKV block's plus the gate/up block's (the latter's dx buffer)."""
+        return self.gu.dx
 
     def forward(self, x, stream=None):
         return self.qkv.forward(x, stream), self.gu.forward(x, stream)
 
     def backward(self, x, dy_qkv, dy_gu, stream=None):
-        self.qkv.backward(x, dy_qkv, stream)
-        self.gu.backward(x, dy_gu, stream)
-        return B.add(self.qkv.dx, self.gu.dx, self.dx, stream=stream)
+        dxq = self.qkv.backward(x, dy_qkv, stream)[0]
+        return self.gu.backward(x, dy_gu, stream, dx_residual=dxq)[0]
 
 
 def build_workload(name, tensors, device="cuda", T=None):
