@@ -142,6 +142,28 @@ def test_layer_parity():
         assert_close(k, v, g[k])
 
 
+def test_layer_attention_gradients_in_place():
+    # dq and dk handed over as the stacked QKV gradient's own planes (no copies) give the
+    # same gradients, bit for bit, as separate tensors copied in
+    T, d, r, ffn, S = 256, 256, 64, 384, 4
+    w = inputs.make_layer(T, d, r, ffn, seed=5)
+    layer = Layer(T, d, r, ffn, S=S, weights=w["p"])
+    x, dout = w["x"].cuda(), w["dout"].cuda()
+    dq, dk = w["dq"].cuda(), w["dk"].cuda()
+    layer.forward(x)
+    layer.backward(x, dout, dq, dk)
+    B.check(layer.qkv.ws)
+    ref = [t.clone() for t in (layer.dx, layer.qkv.dA, layer.qkv.dB, layer.o.dA, layer.o.dB)]
+    layer.dqkv[0].copy_(dq)
+    layer.dqkv[1].copy_(dk)
+    layer.forward(x)
+    layer.backward(x, dout, layer.dqkv[0], layer.dqkv[1])
+    B.check(layer.qkv.ws)
+    got = (layer.dx, layer.qkv.dA, layer.qkv.dB, layer.o.dA, layer.o.dB)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+
+
 def test_svd_pair_parity():
     T, d, r, ffn, S = 256, 256, 64, 320, 4
     w = inputs.make_svd_pair(T, d, r, ffn, seed=3)
