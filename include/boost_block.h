@@ -155,8 +155,8 @@ boost_status boost_block_fwd_swiglu(const boost_block_desc* desc,
  *   res    [T, n]     the residual (device, bf16, 16-byte aligned; disjoint from y, or y
  *                     itself); may be NULL only when T == 0
  *   y      [1, T, n]  out: res + block(x)
- * Errors: as boost_block_fwd, plus BOOST_ERR_INVALID_ARG for k != 1 or a NULL res,
- * BOOST_ERR_ALIGNMENT for a misaligned res. The up-projection always uses its
+ * Errors: as boost_block_fwd, plus BOOST_ERR_INVALID_ARG for k != 1, a NULL res or a
+ * res that overlaps y without being y, BOOST_ERR_ALIGNMENT for a misaligned res. The up-projection always uses its
  * plain-store epilogue here (no TMA stores).
  */
 boost_status boost_block_fwd_residual(const boost_block_desc* desc,
@@ -198,8 +198,8 @@ boost_status boost_block_bwd(const boost_block_desc* desc,
  *   res    [T, d]  the residual gradient (device, bf16, 16-byte aligned; disjoint from
  *                  dx, or dx itself); may be NULL only when T == 0
  *   dx     [T, d]  out: res + the block's input gradient
- * Errors: as boost_block_bwd, plus BOOST_ERR_INVALID_ARG for a NULL res,
- * BOOST_ERR_ALIGNMENT for a misaligned res.
+ * Errors: as boost_block_bwd, plus BOOST_ERR_INVALID_ARG for a NULL res or a res that
+ * overlaps dx without being dx, BOOST_ERR_ALIGNMENT for a misaligned res.
  */
 boost_status boost_block_bwd_residual(const boost_block_desc* desc,
                                       const void* x, const void* gamma, const void* A,

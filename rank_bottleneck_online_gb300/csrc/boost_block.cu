@@ -56,6 +56,12 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Two buffers of `bytes` each that overlap without being the same buffer.
+bool partial_overlap(const void* a, const void* b, uint64_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x != y && x < y + bytes && y < x + bytes;
+}
+
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // --------------------------------------------------------------- devices
@@ -795,6 +801,11 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
     // y = res + block(x): one output group, res shaped like it
     if (D.k != 1 || (D.T > 0 && res == nullptr)) return BOOST_ERR_INVALID_ARG;
     if (res != nullptr && !aligned16(res)) return BOOST_ERR_ALIGNMENT;
+    // the epilogue reads each residual element before writing the same output element,
+    // so res may be y itself, but not a shifted view of it
+    if (res != nullptr && y != nullptr &&
+        partial_overlap(res, y, 2ull * static_cast<uint64_t>(D.T) * static_cast<uint64_t>(D.n)))
+      return BOOST_ERR_INVALID_ARG;
   }
   // With no tokens the [T, ...] tensors are empty and may be NULL.
   st = D.T == 0 ? check_ptrs({A, B}, {gamma, rstd, x, y, h})
@@ -954,6 +965,9 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
     // dx = res + the block's input gradient (res shaped like dx)
     if (gate != nullptr || (D.T > 0 && dx_res == nullptr)) return BOOST_ERR_INVALID_ARG;
     if (dx_res != nullptr && !aligned16(dx_res)) return BOOST_ERR_ALIGNMENT;
+    if (dx_res != nullptr && dx != nullptr &&
+        partial_overlap(dx_res, dx, 2ull * static_cast<uint64_t>(D.T) * static_cast<uint64_t>(D.d)))
+      return BOOST_ERR_INVALID_ARG;
   }
   const bool glu = gate != nullptr;
   if (!D.has_norm && (gamma != nullptr || rstd != nullptr || dgamma != nullptr))

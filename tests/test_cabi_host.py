@@ -237,6 +237,10 @@ def test_residual_entry_point_argument_checks(L):
     assert fwd(ok, 0x60008) == 3                                # misaligned residual
     assert bwd(ok, 0) == 1
     assert bwd(ok, 0x60008) == 3
+    # a residual that overlaps the output without being it (y at 0x50000, dx at 0x6000;
+    # T * n * 2 = 64 KB): rejected; the output itself is allowed only as the same buffer
+    assert fwd(ok, 0x50010) == 1
+    assert bwd(ok, 0x6010) == 1
     empty = B.make_desc(0, 256, 64, 1, 256, S=4)
     wsb0 = B.workspace_bytes(empty) or 1 << 20
     assert fwd(empty, 0, wsb0) == 0
