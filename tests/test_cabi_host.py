@@ -244,3 +244,18 @@ def test_residual_entry_point_argument_checks(L):
     empty = B.make_desc(0, 256, 64, 1, 256, S=4)
     wsb0 = B.workspace_bytes(empty) or 1 << 20
     assert fwd(empty, 0, wsb0) == 0
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c11"), ("c++", "-std=c++17")])
+def test_header_compiles_as_plain_c_and_cpp(lang, std):
+    # the boundary header declares a C ABI: it must parse as C (and as C++) on its own
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                       "boost_block.h")
+    r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, std, hdr],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
