@@ -859,7 +859,7 @@ def _e2e(args, mlp, w, x, dout, T, d, dev):
     return time.perf_counter() - t0, ("cuda_graph" if graph is not None else "eager")
 
 
-# Operations the library runs concurrently with other GEMMs (unless BOOST_FORK_STREAMS=0):
+# Operations the library runs concurrently with other GEMMs when BOOST_FORK_STREAMS=1:
 # dB and dA on forked streams beside dx on the caller's stream, the gamma fold beside
 # the statistics. Their event intervals include time shared with the concurrent work,
 # so they are not kernel durations.
@@ -868,7 +868,10 @@ OVERLAPPED_OPS = ("gemm_wgrad_B", "gemm_wgrad_A", "splitk_sum", "splitk_finalize
 
 
 def _forked():
-    return os.environ.get("BOOST_FORK_STREAMS", "1") != "0"
+    try:
+        return int(os.environ.get("BOOST_FORK_STREAMS", "0")) != 0
+    except ValueError:
+        return False
 
 
 def dominant_kernel(prof, overlapped):

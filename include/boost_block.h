@@ -25,7 +25,8 @@
  *   process, created on first use: a second stream and two events that let one
  *   GEMM run as two concurrent launches over disjoint rows or columns
  *   ("co-scheduling": a launch of 8-CTA clusters plus a CTA-pair launch on the
- *   SMs no cluster fits); two more streams and three events on which the backward
+ *   SMs no cluster fits); two more streams and three events on which the backward,
+ *   when the environment sets BOOST_FORK_STREAMS=1 (off by default),
  *   runs its dB and dA GEMMs concurrently with dx; and cached cluster-occupancy
  *   counts (boost_rmsnorm_rstd_noalloc adds its fixed array, below).
  * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default

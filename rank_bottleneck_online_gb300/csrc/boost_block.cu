@@ -183,16 +183,20 @@ struct Plan {
 };
 
 // Split-K choice for a weight gradient: minimise the estimated time
-//   waves(s) * k-blocks per split * t_kb  +  partial bytes / HBM bandwidth,
+//   waves(s) * k-blocks per split * t_kb  +  partial bytes / HBM bandwidth  +  t_fix,
 // where a wave is one pass of `groups` CTA groups over the tile list, t_kb is the
 // time of one 64-deep k-block of a 256x256 tile on a CTA pair (about 0.5 us at the
-// measured ~1.2-1.3 PFLOP/s), and the fp32 partials are written once and read once.
+// measured ~1.2-1.3 PFLOP/s), the fp32 partials are written once and read once, and
+// t_fix (10 us) is the finaliser's own launch and ramp beyond its bytes. (Without t_fix
+// the 1B block's two weight gradients split 5 ways. Unsplit measured 1.2% faster on the
+// step: 0.585 -> 0.578 ms. The other workloads' plans do not change.)
 int env_int(const char* name, int dflt);
 
 void choose_splits(int64_t tiles, int64_t nkb, int groups, int64_t out_elems, int& splits,
                    int& kbps) {
   constexpr double kTkb = 0.5e-6;          // seconds per k-block per tile
   constexpr double kHbm = 6.0e12;          // bytes per second
+  constexpr double kFix = 10e-6;           // seconds: the finaliser beyond its bytes
   splits = 1;
   kbps = static_cast<int>(nkb);
   static const int forced = env_int("BOOST_SPLITK", 0);   // > 0: this many splits (tuning)
@@ -209,7 +213,7 @@ void choose_splits(int64_t tiles, int64_t nkb, int groups, int64_t out_elems, in
     const int64_t s_eff = cdiv(nkb, per);
     const int64_t waves = cdiv(tiles * s_eff, groups);
     double cost = static_cast<double>(waves * per) * kTkb;
-    if (s_eff > 1) cost += 2.0 * 4.0 * static_cast<double>(s_eff) * out_elems / kHbm;
+    if (s_eff > 1) cost += 2.0 * 4.0 * static_cast<double>(s_eff) * out_elems / kHbm + kFix;
     if (cost < best * (1.0 - 1e-6)) {
       best = cost;
       splits = static_cast<int>(s_eff);
@@ -592,8 +596,13 @@ cudaError_t launch_gemm_cols(const Shape& sh, int mode, const GemmParams& g_in, 
 // backward GEMMs after the dual kernel (dB and dA on the extra streams, dx on the
 // caller's), and the statistics and the gamma fold before a normed block's GEMMs.
 // Each persistent GEMM fills the GPU on its own; running them concurrently lets one's
-// last, partly filled wave overlap the next one's start. BOOST_FORK_STREAMS=0 turns it
-// off. Per-device streams and events, created on first use; one fork/join at a time.
+// last, partly filled wave overlap the next one's start. Off by default
+// (BOOST_FORK_STREAMS=1 turns it on): since every GEMM's cluster launch has a
+// co-scheduled pair launch on the remaining SMs, concurrent GEMMs mostly contend for
+// SMs and cluster placement, and the one-stream order measured faster (7B MLP
+// 3.412-3.421 -> 3.384-3.402 ms, 1B block 0.591-0.594 -> 0.582 ms, 13B layer equal,
+// 40B pair about 1% slower). Per-device streams and events, created on first use; one
+// fork/join at a time.
 struct ForkStreams {
   cudaStream_t aux[2] = {nullptr, nullptr};
   cudaEvent_t fork = nullptr, join[2] = {nullptr, nullptr};
@@ -630,7 +639,7 @@ ForkStreams* fork_streams() {
 class StreamFork {
  public:
   explicit StreamFork(cudaStream_t s) : s_(s) {
-    static const int on = env_int("BOOST_FORK_STREAMS", 1);
+    static const int on = env_int("BOOST_FORK_STREAMS", 0);
     if (!on || (bs_ = fork_streams()) == nullptr) return;
     lk_ = std::unique_lock<std::mutex>(bs_->order);
     if (cudaEventRecord(bs_->fork, s_) != cudaSuccess ||

@@ -367,7 +367,7 @@ def test_two_host_threads_on_their_own_streams_match_serial_runs():
     # and co-scheduling streams are used one fork/join sequence at a time
     import threading
 
-    shape = (4352, 512, 512, 2, 1024, 4)          # co-scheduled rows and forked backward
+    shape = (4352, 512, 512, 2, 1024, 4)          # co-scheduled rows
     blocks, data = [], []
     for seed in (41, 42):
         T, d, r, k, n, S = shape
@@ -433,3 +433,45 @@ def test_seeded_random_shapes_parity(case):
     assert_close("dx", blk.dx, gr["dx"])
     assert_close("dA", blk.dA, gr["dA"])
     assert_close("dB", blk.dB, gr["dB"])
+
+
+def test_forked_backward_streams_give_the_same_results():
+    # BOOST_FORK_STREAMS=1 (read once per process) runs dB and dA on forked streams beside
+    # dx, and the fold beside the statistics: a child process with it set gives the
+    # default one-stream results bit for bit (same kernels, same split plans)
+    import hashlib
+    import subprocess
+    import sys
+
+    shape = (4352, 512, 512, 2, 1024, 4)          # co-scheduled rows, split-K wgrads
+    code = (
+        "import hashlib, sys, torch\n"
+        "sys.path.insert(0, '.')\n"
+        "from rank_bottleneck_online_gb300 import inputs, binding as B\n"
+        "from rank_bottleneck_online_gb300.block import Block\n"
+        f"T, d, r, k, n, S = {shape}\n"
+        "w = inputs.make_block(T, d, r, k, n, seed=43)\n"
+        "blk = Block(T, d, r, k, n, S=S, weights=w)\n"
+        "x, dy = w['x'].cuda(), w['dy'].cuda()\n"
+        "blk.forward(x); blk.backward(x, dy); B.check(blk.ws)\n"
+        "h = hashlib.sha256()\n"
+        "for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma):\n"
+        "    h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())\n"
+        "print(h.hexdigest())\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, BOOST_FORK_STREAMS="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    forked = r.stdout.strip().splitlines()[-1]
+    T, d, r_, k, n, S = shape
+    w = inputs.make_block(T, d, r_, k, n, seed=43)
+    blk = Block(T, d, r_, k, n, S=S, weights=w)
+    x, dy = w["x"].cuda(), w["dy"].cuda()
+    blk.forward(x)
+    blk.backward(x, dy)
+    B.check(blk.ws)
+    h = hashlib.sha256()
+    for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma):
+        h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
+    assert h.hexdigest() == forked
