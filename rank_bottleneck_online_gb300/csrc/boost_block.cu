@@ -636,11 +636,15 @@ ForkStreams* fork_streams() {
   return &b;
 }
 
+bool forks_enabled() {
+  static const int on = env_int("BOOST_FORK_STREAMS", 0);
+  return on != 0;
+}
+
 class StreamFork {
  public:
   explicit StreamFork(cudaStream_t s) : s_(s) {
-    static const int on = env_int("BOOST_FORK_STREAMS", 0);
-    if (!on || (bs_ = fork_streams()) == nullptr) return;
+    if (!forks_enabled() || (bs_ = fork_streams()) == nullptr) return;
     lk_ = std::unique_lock<std::mutex>(bs_->order);
     if (cudaEventRecord(bs_->fork, s_) != cudaSuccess ||
         cudaStreamWaitEvent(bs_->aux[0], bs_->fork, 0) != cudaSuccess ||
@@ -840,7 +844,17 @@ boost_status block_fwd_impl(const boost_block_desc* desc, const void* x, const v
   float* rs = nullptr;
   float* zpart = payload;                                   // [S, T, kr]
   float* ssq_x = btp && D.has_norm ? payload + D.S * D.T * P.kr : nullptr;   // [S, T]
-  if (D.has_norm) {
+  if (D.has_norm && !forks_enabled()) {
+    // the statistics and the fold in one launch (under the emulated exchange the shard
+    // sums of squares go into the payload)
+    rs = rstd ? rstd : ws_at<float>(ws, P.off_rstd);
+    ProfScope ps(s, K_STATS_FOLD, 0.0, stats_bytes(P, D.S) + fold_bytes(P));
+    if (launch_stats_fold(x, D.T, D.d, D.S, D.eps, btp ? ssq_x : ws_at<float>(ws, P.off_ssq),
+                          btp ? ws_at<float>(ws, P.off_rstd) : rs, gamma, A,
+                          ws_at<void>(ws, P.off_Ap), P.kr, s) != cudaSuccess)
+      return BOOST_ERR_CUDA;
+    Ap = ws_at<void>(ws, P.off_Ap);
+  } else if (D.has_norm) {
     rs = rstd ? rstd : ws_at<float>(ws, P.off_rstd);
     cudaError_t e;
     StreamFork fork(s);   // the fold runs beside the statistics
@@ -1006,7 +1020,16 @@ boost_status block_bwd_impl(const boost_block_desc* desc, const void* x, const v
 
   const void* Ap = A;
   const float* rs = nullptr;
-  if (D.has_norm) {
+  if (D.has_norm && rstd == nullptr && !forks_enabled()) {
+    // the row scale recomputed: the statistics and the fold in one launch
+    float* r = ws_at<float>(ws, P.off_rstd);
+    ProfScope ps(s, K_STATS_FOLD, 0.0, stats_bytes(P, D.S) + fold_bytes(P));
+    if (launch_stats_fold(x, D.T, D.d, D.S, D.eps, ws_at<float>(ws, P.off_ssq), r, gamma, A,
+                          ws_at<void>(ws, P.off_Ap), P.kr, s) != cudaSuccess)
+      return BOOST_ERR_CUDA;
+    rs = r;
+    Ap = ws_at<void>(ws, P.off_Ap);
+  } else if (D.has_norm) {
     std::unique_ptr<StreamFork> fork;   // the fold beside the statistics, when both run
     cudaStream_t sf = s;
     if (rstd == nullptr) {

@@ -24,6 +24,10 @@ cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, flo
                                  float* ssq, float* rstd, cudaStream_t stream);
 cudaError_t launch_fold_gamma(const void* gamma, const void* A, void* Ap, int64_t d, int64_t kr,
                               cudaStream_t stream);
+// the statistics and the gamma fold of a normed block in one launch
+cudaError_t launch_stats_fold(const void* x, int64_t T, int64_t d, int S, float eps, float* ssq,
+                              float* rstd, const void* gamma, const void* A, void* Ap, int64_t kr,
+                              cudaStream_t stream);
 cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64_t T,
                               int64_t kr, int64_t d, float eps, int act, void* a, float* rstd,
                               cudaStream_t stream);

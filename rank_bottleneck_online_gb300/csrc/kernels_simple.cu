@@ -48,12 +48,9 @@ __device__ __forceinline__ float silu_grad_f(float z) {
 // Online-RMSNorm statistics (BOOST technical summary §2.2): one warp per row.
 // ssq[s, t] is the fp32 sum of squares over shard s = columns [s*w, (s+1)*w);
 // the shards are then combined once, in index order, into rstd[t].
-__global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
-    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
-    float* __restrict__ ssq, float* __restrict__ rstd) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= T) return;
+__device__ __forceinline__ void stats_row(const __nv_bfloat16* __restrict__ x, int64_t T,
+                                          int64_t d, int S, float eps, float* __restrict__ ssq,
+                                          float* __restrict__ rstd, int64_t row, int lane) {
   const __nv_bfloat16* xr = x + row * d;
   const int64_t w = d / S;
   float total = 0.0f;
@@ -91,6 +88,13 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
     total += part;  // the single combine, in shard order
   }
   if (lane == 0) rstd[row] = 1.0f / sqrtf(total / static_cast<float>(d) + eps);
+}
+
+__global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
+    float* __restrict__ ssq, float* __restrict__ rstd) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  if (row < T) stats_row(x, T, d, S, eps, ssq, rstd, row, threadIdx.x & 31);
 }
 
 // The reduction standing in for the bottleneck-aware TP all-reduce (BOOST technical
@@ -135,12 +139,10 @@ __global__ void __launch_bounds__(kThreads) btp_reduce_kernel(
 // one shard for the whole warp, so a lane can issue eight loads before it reduces (a
 // row's loads in flight instead of two pieces per shard) and the shard boundaries stay
 // warp-uniform. Shards are reduced and combined in index order.
-__global__ void __launch_bounds__(kThreads) rmsnorm_stats_wide_kernel(
-    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
-    float* __restrict__ ssq, float* __restrict__ rstd) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= T) return;
+__device__ __forceinline__ void stats_row_wide(const __nv_bfloat16* __restrict__ x, int64_t T,
+                                               int64_t d, int S, float eps,
+                                               float* __restrict__ ssq, float* __restrict__ rstd,
+                                               int64_t row, int lane) {
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * d) + lane;
   const int nj = static_cast<int>(d / 256);          // pieces per lane
   const int jps = static_cast<int>(d / S / 256);     // pieces per lane per shard
@@ -174,17 +176,25 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_stats_wide_kernel(
   if (lane == 0) rstd[row] = 1.0f / sqrtf(total / static_cast<float>(d) + eps);
 }
 
+__global__ void __launch_bounds__(kThreads) rmsnorm_stats_wide_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
+    float* __restrict__ ssq, float* __restrict__ rstd) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  if (row < T) stats_row_wide(x, T, d, S, eps, ssq, rstd, row, threadIdx.x & 31);
+}
+
 // A'[j, m] = bf16(gamma_j * A[j, m]); the product of two bf16 values is exact in fp32.
 // A grid-stride loop over the 16-byte pieces of A; each thread has kFoldUnroll pieces
 // (kThreads pieces apart) in flight before it scales and stores them.
 constexpr int kFoldUnroll = 4;
 
-__global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
-    const __nv_bfloat16* __restrict__ gamma, const uint4* __restrict__ A, uint4* __restrict__ Ap,
-    int64_t nvec, int64_t row_vecs) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * kFoldUnroll;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kFoldUnroll + threadIdx.x;
-       base < nvec; base += stride) {
+// (block `blk` of `nblk` blocks taking part in the fold)
+__device__ __forceinline__ void fold_part(const __nv_bfloat16* __restrict__ gamma,
+                                          const uint4* __restrict__ A, uint4* __restrict__ Ap,
+                                          int64_t nvec, int64_t row_vecs, int64_t blk,
+                                          int64_t nblk) {
+  const int64_t stride = nblk * kThreads * kFoldUnroll;
+  for (int64_t base = blk * kThreads * kFoldUnroll + threadIdx.x; base < nvec; base += stride) {
     uint4 u[kFoldUnroll];
 #pragma unroll
     for (int k = 0; k < kFoldUnroll; ++k) {
@@ -202,6 +212,33 @@ __global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
       for (int e = 0; e < 8; ++e) f[e] *= g;
       Ap[i] = pack8(f);
     }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
+    const __nv_bfloat16* __restrict__ gamma, const uint4* __restrict__ A, uint4* __restrict__ Ap,
+    int64_t nvec, int64_t row_vecs) {
+  fold_part(gamma, A, Ap, nvec, row_vecs, blockIdx.x, gridDim.x);
+}
+
+// The statistics and the gamma fold of a normed block in one launch: they are
+// independent and both bandwidth-bound, so the fold's blocks fill the statistics' tail
+// and one launch replaces two. Blocks [0, stat_blocks) take rows of x (one warp per row),
+// the rest take pieces of A.
+__global__ void __launch_bounds__(kThreads) stats_fold_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
+    float* __restrict__ ssq, float* __restrict__ rstd, int wide, int64_t stat_blocks,
+    const __nv_bfloat16* __restrict__ gamma, const uint4* __restrict__ A, uint4* __restrict__ Ap,
+    int64_t nvec, int64_t row_vecs) {
+  const int64_t b = blockIdx.x;
+  if (b < stat_blocks) {
+    const int64_t row = b * (kThreads / 32) + (threadIdx.x >> 5);
+    if (row < T) {
+      if (wide) stats_row_wide(x, T, d, S, eps, ssq, rstd, row, threadIdx.x & 31);
+      else stats_row(x, T, d, S, eps, ssq, rstd, row, threadIdx.x & 31);
+    }
+  } else {
+    fold_part(gamma, A, Ap, nvec, row_vecs, b - stat_blocks, gridDim.x - stat_blocks);
   }
 }
 
@@ -411,6 +448,23 @@ cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64
   if (T == 0) return cudaSuccess;
   btp_reduce_kernel<<<grid_for(T * (kr / 8), kThreads), kThreads, 0, stream>>>(
       zpart, ssq, S, T, kr, d, eps, act, static_cast<uint4*>(a), rstd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats_fold(const void* x, int64_t T, int64_t d, int S, float eps, float* ssq,
+                              float* rstd, const void* gamma, const void* A, void* Ap, int64_t kr,
+                              cudaStream_t stream) {
+  if (T == 0) return launch_fold_gamma(gamma, A, Ap, d, kr, stream);
+  if (d * kr == 0) return launch_rmsnorm_stats(x, T, d, S, eps, ssq, rstd, stream);
+  const int rows_per_block = kThreads / 32;
+  const int64_t stat_blocks = (T + rows_per_block - 1) / rows_per_block;
+  const int64_t nvec = d * (kr / 8);
+  const int64_t fold_blocks = grid_for(nvec, kThreads * kFoldUnroll);
+  const int wide = ((d / S) % 256 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) ? 1 : 0;
+  stats_fold_kernel<<<static_cast<unsigned>(stat_blocks + fold_blocks), kThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd, wide, stat_blocks,
+      static_cast<const __nv_bfloat16*>(gamma), static_cast<const uint4*>(A),
+      static_cast<uint4*>(Ap), nvec, kr / 8);
   return cudaGetLastError();
 }
 

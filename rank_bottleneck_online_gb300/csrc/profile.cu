@@ -22,7 +22,7 @@ const char* const kNames[K_COUNT] = {
     "gemm_dual",     "gemm_wgrad_B",   "gemm_wgrad_A",   "gemm_dx",
     "splitk_sum",    "splitk_finalize_dA", "dgamma_reduce", "swiglu_fwd",
     "swiglu_bwd",    "add",            "wait_probe",    "gemm_dx_swiglu",
-    "gemm_up_swiglu", "gemm_down_partials", "btp_exchange_reduce"};
+    "gemm_up_swiglu", "gemm_down_partials", "btp_exchange_reduce", "rmsnorm_stats_fold"};
 
 struct Pending {
   int id;

@@ -27,6 +27,7 @@ enum KernelId : int {
   K_UP_GLU,
   K_BTP_PARTIAL,
   K_BTP_REDUCE,
+  K_STATS_FOLD,
   K_COUNT
 };
 
