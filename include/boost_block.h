@@ -33,7 +33,11 @@
  *   stream): work on the library's other streams is forked from `stream` and
  *   joined back to it with events, so everything a call enqueues is ordered after
  *   earlier work on `stream` and before later work on it. Calls may be captured into
- *   CUDA graphs (the fork and join become part of the capture). Every argument
+ *   CUDA graphs (the fork and join become part of the capture). Kernels are launched
+ *   as programmatic dependent launches (unless the environment sets BOOST_PDL=0):
+ *   each may start its prologue while the kernel before it on the stream finishes,
+ *   but waits for that kernel's completion before it reads or writes global memory,
+ *   so the ordering above holds for any earlier work. Every argument
  *   is validated on the host before anything is enqueued: a call that returns
  *   BOOST_ERR_INVALID_ARG, _UNSUPPORTED_SHAPE, _ALIGNMENT or _WORKSPACE has
  *   enqueued nothing; BOOST_ERR_CUDA (a launch refused by the runtime) may

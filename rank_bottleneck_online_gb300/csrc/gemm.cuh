@@ -1050,6 +1050,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, MODE, CG, MCM, MCN>::kThreads, 1)
   if constexpr (CL > 1) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Everything above touches only shared memory, TMEM and the kernel parameters, so it
+  // may overlap the previous kernel on the stream; global memory waits for it. The next
+  // kernel may be scheduled from here: its CTAs fit on an SM only once this kernel's CTA
+  // there has exited, and this CTA's TMEM is already held.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

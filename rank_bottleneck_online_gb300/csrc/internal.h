@@ -19,6 +19,11 @@ cudaError_t launch_gemm(int bn, int mode, int cg, int mcm, int mcn, const GemmPa
 // Clusters of that configuration resident at once (the persistent grid size).
 int gemm_resident(int bn, int mode, int cg, int mcm, int mcn, int num_sms);
 
+// Launches carry the programmatic-stream-serialisation attribute (the next kernel's
+// prologue overlaps this one's tail; every kernel waits in griddep_wait before it
+// touches global memory) unless the environment sets BOOST_PDL=0.
+bool pdl_enabled();
+
 // ------------------------------------------------------ CUDA-core kernels
 cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, float eps,
                                  float* ssq, float* rstd, cudaStream_t stream);

@@ -5,6 +5,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <utility>
+
 #include "internal.h"
 
 namespace boost_gb300 {
@@ -29,6 +32,31 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// The first statement of every kernel here: wait for the kernel before it on the
+// stream (a no-op unless the launch carried a programmatic dependency), then let the
+// next one be scheduled. Both precede any global memory access.
+__device__ __forceinline__ void pdl_enter() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
+// Launch `kern` on `stream`, with the programmatic-stream-serialisation attribute
+// when enabled.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), int64_t grid, cudaStream_t stream,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // logistic(z) with the hardware exp2 and a fast reciprocal divide, the same expression
@@ -93,6 +121,7 @@ __device__ __forceinline__ void stats_row(const __nv_bfloat16* __restrict__ x, i
 __global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
     float* __restrict__ ssq, float* __restrict__ rstd) {
+  pdl_enter();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
   if (row < T) stats_row(x, T, d, S, eps, ssq, rstd, row, threadIdx.x & 31);
 }
@@ -105,6 +134,7 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_stats_kernel(
 __global__ void __launch_bounds__(kThreads) btp_reduce_kernel(
     const float* __restrict__ zpart, const float* __restrict__ ssq, int S, int64_t T,
     int64_t kr, int64_t d, float eps, int act, uint4* __restrict__ a, float* __restrict__ rstd) {
+  pdl_enter();
   const int64_t nv = kr / 8;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < T * nv;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
@@ -179,6 +209,7 @@ __device__ __forceinline__ void stats_row_wide(const __nv_bfloat16* __restrict__
 __global__ void __launch_bounds__(kThreads) rmsnorm_stats_wide_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t T, int64_t d, int S, float eps,
     float* __restrict__ ssq, float* __restrict__ rstd) {
+  pdl_enter();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
   if (row < T) stats_row_wide(x, T, d, S, eps, ssq, rstd, row, threadIdx.x & 31);
 }
@@ -218,6 +249,7 @@ __device__ __forceinline__ void fold_part(const __nv_bfloat16* __restrict__ gamm
 __global__ void __launch_bounds__(kThreads) fold_gamma_kernel(
     const __nv_bfloat16* __restrict__ gamma, const uint4* __restrict__ A, uint4* __restrict__ Ap,
     int64_t nvec, int64_t row_vecs) {
+  pdl_enter();
   fold_part(gamma, A, Ap, nvec, row_vecs, blockIdx.x, gridDim.x);
 }
 
@@ -230,6 +262,7 @@ __global__ void __launch_bounds__(kThreads) stats_fold_kernel(
     float* __restrict__ ssq, float* __restrict__ rstd, int wide, int64_t stat_blocks,
     const __nv_bfloat16* __restrict__ gamma, const uint4* __restrict__ A, uint4* __restrict__ Ap,
     int64_t nvec, int64_t row_vecs) {
+  pdl_enter();
   const int64_t b = blockIdx.x;
   if (b < stat_blocks) {
     const int64_t row = b * (kThreads / 32) + (threadIdx.x >> 5);
@@ -244,6 +277,7 @@ __global__ void __launch_bounds__(kThreads) stats_fold_kernel(
 
 __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(
     const uint4* __restrict__ g, const uint4* __restrict__ u, uint4* __restrict__ h, int64_t nvec) {
+  pdl_enter();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
     float fg[8], fu[8], fh[8];
@@ -258,6 +292,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(
 __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(
     const uint4* __restrict__ g, const uint4* __restrict__ u, const uint4* __restrict__ dh,
     uint4* __restrict__ dg, uint4* __restrict__ du, int64_t nvec) {
+  pdl_enter();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
     float fg[8], fu[8], fd[8], og[8], ou[8];
@@ -276,6 +311,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(
 
 __global__ void __launch_bounds__(kThreads) add_kernel(const uint4* a, const uint4* b, uint4* out,
                                                        int64_t nvec) {
+  pdl_enter();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
     float fa[8], fb[8];
@@ -296,6 +332,7 @@ constexpr int kMaxSplits = 8;
 template <int MAXS>
 __global__ void __launch_bounds__(kThreads) splitk_sum_bf16_kernel(
     const float4* __restrict__ part, int splits, int64_t count4, uint2* __restrict__ out) {
+  pdl_enter();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < count4;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
     float4 v[MAXS];
@@ -322,6 +359,7 @@ __global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
     const float* __restrict__ part, int splits, int64_t d, int64_t kr,
     const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ A,
     __nv_bfloat16* __restrict__ dA, __nv_bfloat16* __restrict__ dgamma) {
+  pdl_enter();
   __shared__ float wsum[kThreads / 32];
   const int64_t j = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -387,6 +425,7 @@ __global__ void __launch_bounds__(kThreads) splitk_finalize_dA_kernel(
 // dgamma_j = bf16(sum_t dgpart[t][j]), tiles summed in index order.
 __global__ void __launch_bounds__(kThreads) dgamma_reduce_kernel(
     const float* __restrict__ dgpart, int ntiles, int64_t d, __nv_bfloat16* __restrict__ dgamma) {
+  pdl_enter();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if (j >= d) return;
   float acc = 0.0f;
@@ -428,27 +467,30 @@ int grid_for(int64_t work, int per_block) {
 
 }  // namespace
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("BOOST_PDL");
+    return e == nullptr || std::atoi(e) != 0;
+  }();
+  return on;
+}
+
 cudaError_t launch_rmsnorm_stats(const void* x, int64_t T, int64_t d, int S, float eps,
                                  float* ssq, float* rstd, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int rows_per_block = kThreads / 32;
   const int64_t grid = (T + rows_per_block - 1) / rows_per_block;
-  if ((d / S) % 256 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0)
-    rmsnorm_stats_wide_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
-  else
-    rmsnorm_stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
-  return cudaGetLastError();
+  const bool wide = (d / S) % 256 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  return launch_k(wide ? rmsnorm_stats_wide_kernel : rmsnorm_stats_kernel, grid, stream,
+                  static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd);
 }
 
 cudaError_t launch_btp_reduce(const float* zpart, const float* ssq, int S, int64_t T,
                               int64_t kr, int64_t d, float eps, int act, void* a, float* rstd,
                               cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  btp_reduce_kernel<<<grid_for(T * (kr / 8), kThreads), kThreads, 0, stream>>>(
+  return launch_k(btp_reduce_kernel, grid_for(T * (kr / 8), kThreads), stream,
       zpart, ssq, S, T, kr, d, eps, act, static_cast<uint4*>(a), rstd);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_stats_fold(const void* x, int64_t T, int64_t d, int S, float eps, float* ssq,
@@ -461,48 +503,43 @@ cudaError_t launch_stats_fold(const void* x, int64_t T, int64_t d, int S, float 
   const int64_t nvec = d * (kr / 8);
   const int64_t fold_blocks = grid_for(nvec, kThreads * kFoldUnroll);
   const int wide = ((d / S) % 256 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) ? 1 : 0;
-  stats_fold_kernel<<<static_cast<unsigned>(stat_blocks + fold_blocks), kThreads, 0, stream>>>(
+  return launch_k(stats_fold_kernel, stat_blocks + fold_blocks, stream,
       static_cast<const __nv_bfloat16*>(x), T, d, S, eps, ssq, rstd, wide, stat_blocks,
       static_cast<const __nv_bfloat16*>(gamma), static_cast<const uint4*>(A),
       static_cast<uint4*>(Ap), nvec, kr / 8);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_fold_gamma(const void* gamma, const void* A, void* Ap, int64_t d, int64_t kr,
                               cudaStream_t stream) {
   if (d * kr == 0) return cudaSuccess;
   const int64_t nvec = d * (kr / 8);
-  fold_gamma_kernel<<<grid_for(nvec, kThreads * kFoldUnroll), kThreads, 0, stream>>>(
+  return launch_k(fold_gamma_kernel, grid_for(nvec, kThreads * kFoldUnroll), stream,
       static_cast<const __nv_bfloat16*>(gamma), static_cast<const uint4*>(A),
       static_cast<uint4*>(Ap), nvec, kr / 8);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_fwd(const void* g, const void* u, void* h, int64_t count,
                               cudaStream_t stream) {
   if (count == 0) return cudaSuccess;
-  swiglu_fwd_kernel<<<grid_for(count / 8, kThreads), kThreads, 0, stream>>>(
+  return launch_k(swiglu_fwd_kernel, grid_for(count / 8, kThreads), stream,
       static_cast<const uint4*>(g), static_cast<const uint4*>(u), static_cast<uint4*>(h),
       count / 8);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_bwd(const void* g, const void* u, const void* dh, void* dg, void* du,
                               int64_t count, cudaStream_t stream) {
   if (count == 0) return cudaSuccess;
-  swiglu_bwd_kernel<<<grid_for(count / 8, kThreads), kThreads, 0, stream>>>(
+  return launch_k(swiglu_bwd_kernel, grid_for(count / 8, kThreads), stream,
       static_cast<const uint4*>(g), static_cast<const uint4*>(u), static_cast<const uint4*>(dh),
       static_cast<uint4*>(dg), static_cast<uint4*>(du), count / 8);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_add(const void* a, const void* b, void* out, int64_t count,
                        cudaStream_t stream) {
   if (count == 0) return cudaSuccess;
-  add_kernel<<<grid_for(count / 8, kThreads), kThreads, 0, stream>>>(
+  return launch_k(add_kernel, grid_for(count / 8, kThreads), stream,
       static_cast<const uint4*>(a), static_cast<const uint4*>(b), static_cast<uint4*>(out),
       count / 8);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_sum_bf16(const float* part, int splits, int64_t count, void* out,
@@ -510,9 +547,8 @@ cudaError_t launch_splitk_sum_bf16(const float* part, int splits, int64_t count,
   if (splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;
   if (count == 0) return cudaSuccess;
   const auto kern = splits <= 4 ? splitk_sum_bf16_kernel<4> : splitk_sum_bf16_kernel<kMaxSplits>;
-  kern<<<grid_for(count / 4, kThreads), kThreads, 0, stream>>>(
+  return launch_k(kern, grid_for(count / 4, kThreads), stream,
       reinterpret_cast<const float4*>(part), splits, count / 4, static_cast<uint2*>(out));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_finalize_dA(const float* part, int splits, int64_t d, int64_t kr,
@@ -522,19 +558,17 @@ cudaError_t launch_splitk_finalize_dA(const float* part, int splits, int64_t d, 
   if (d == 0) return cudaSuccess;
   const auto kern =
       splits <= 4 ? splitk_finalize_dA_kernel<4> : splitk_finalize_dA_kernel<kMaxSplits>;
-  kern<<<static_cast<unsigned>(d), kThreads, 0, stream>>>(
+  return launch_k(kern, d, stream,
       part, splits, d, kr, static_cast<const __nv_bfloat16*>(gamma),
       static_cast<const __nv_bfloat16*>(A), static_cast<__nv_bfloat16*>(dA),
       static_cast<__nv_bfloat16*>(dgamma));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_dgamma_reduce(const float* dgpart, int ntiles, int64_t d, void* dgamma,
                                  cudaStream_t stream) {
   if (d == 0) return cudaSuccess;
-  dgamma_reduce_kernel<<<static_cast<unsigned>((d + kThreads - 1) / kThreads), kThreads, 0,
-                         stream>>>(dgpart, ntiles, d, static_cast<__nv_bfloat16*>(dgamma));
-  return cudaGetLastError();
+  return launch_k(dgamma_reduce_kernel, (d + kThreads - 1) / kThreads, stream,
+      dgpart, ntiles, d, static_cast<__nv_bfloat16*>(dgamma));
 }
 
 cudaError_t launch_wait_timeout_probe(DeviceError* err, uint64_t limit_ns, cudaStream_t stream) {

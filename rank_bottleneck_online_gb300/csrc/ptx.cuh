@@ -98,6 +98,20 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, Dev
   return bounded_wait_slow(bar, parity, err, where, limit_ns);
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// (PTX griddepcontrol, sm_90 and later.) `griddep_wait` blocks until every grid this
+// one depends on has completed and its writes are visible; without a programmatic
+// dependency on the launch it returns at once. `griddep_launch_dependents` lets the
+// next grid on the stream be scheduled (its CTAs run up to their own griddep_wait)
+// once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
