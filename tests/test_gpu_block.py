@@ -477,3 +477,60 @@ def test_forked_backward_streams_give_the_same_results():
     for t in (blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma):
         h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
     assert h.hexdigest() == forked
+
+
+_HASH_CHILD = (
+    "import hashlib, sys, torch\n"
+    "sys.path.insert(0, '.')\n"
+    "from rank_bottleneck_online_gb300 import inputs, binding as B\n"
+    "from rank_bottleneck_online_gb300.block import Block, MLP\n"
+    "blk_shape, mlp_shape, graph = {blk!r}, {mlp!r}, {graph!r}\n"
+    "T, d, r, k, n, S = blk_shape\n"
+    "w = inputs.make_block(T, d, r, k, n, seed=43)\n"
+    "blk = Block(T, d, r, k, n, S=S, weights=w)\n"
+    "x, dy = w['x'].cuda(), w['dy'].cuda()\n"
+    "T2, d2, r2, ffn2, S2 = mlp_shape\n"
+    "wm = inputs.make_mlp(T2, d2, r2, ffn2, seed=44)\n"
+    "m = MLP(T2, d2, r2, ffn2, S=S2, weights=wm)\n"
+    "xm, dout = wm['x'].cuda(), wm['dout'].cuda()\n"
+    "def step():\n"
+    "    blk.forward(x); blk.backward(x, dy)\n"
+    "    m.forward(xm); m.backward(xm, dout)\n"
+    "step(); torch.cuda.synchronize()\n"
+    "outs = [blk.y, blk.dx, blk.dA, blk.dB, blk.dgamma, m.out, m.dy1,\n"
+    "        *m.grads().values()]\n"
+    "if graph:\n"
+    "    g = torch.cuda.CUDAGraph()\n"
+    "    with torch.cuda.graph(g):\n"
+    "        step()\n"
+    "    for t in outs:\n"
+    "        t.zero_()\n"
+    "    g.replay(); torch.cuda.synchronize()\n"
+    "B.check(blk.ws); B.check(m.gu.ws); B.check(m.dn.ws)\n"
+    "h = hashlib.sha256()\n"
+    "for t in outs:\n"
+    "    h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())\n"
+    "print(h.hexdigest())\n")
+
+
+def _child_hash(env_over, graph):
+    import subprocess
+    import sys
+
+    code = _HASH_CHILD.format(blk=(4352, 512, 512, 2, 1024, 4),   # co-scheduled, split-K
+                              mlp=(2304, 512, 256, 1536, 4), graph=graph)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root,
+                       env=dict(os.environ, **env_over), capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return r.stdout.strip().splitlines()[-1]
+
+
+def test_programmatic_launches_give_the_same_results():
+    # every kernel is a programmatic dependent launch unless BOOST_PDL=0 (read once per
+    # process). A CUDA graph of the block and MLP steps replayed with them (outputs zeroed
+    # first) gives plain eager launches' results bit for bit.
+    plain = _child_hash({"BOOST_PDL": "0"}, graph=False)
+    assert _child_hash({"BOOST_PDL": "1"}, graph=True) == plain
+    assert _child_hash({"BOOST_PDL": "1"}, graph=False) == plain
