@@ -867,11 +867,16 @@ OVERLAPPED_OPS = ("gemm_wgrad_B", "gemm_wgrad_A", "splitk_sum", "splitk_finalize
                   "dgamma_reduce", "gemm_dx", "gemm_dx_swiglu", "fold_gamma", "rmsnorm_stats")
 
 
-def _forked():
+def _env_flag(name, default):
+    """The library's reading of an on/off environment switch (atoi: non-zero is on)."""
     try:
-        return int(os.environ.get("BOOST_FORK_STREAMS", "0")) != 0
+        return int(os.environ.get(name, str(default))) != 0
     except ValueError:
         return False
+
+
+def _forked():
+    return _env_flag("BOOST_FORK_STREAMS", 0)
 
 
 def dominant_kernel(prof, overlapped):
@@ -953,7 +958,9 @@ def _report(args, world, prof, prof_kernels, clocks, ms_total, e2e_s, bi, bo, T,
                    **({k: v for k, v in _cfg(args.workload).items() if k in ("k", "n", "kind")}),
                    "parallelism": "single",
                    "l2": "inputs larger than L2 (no flush)",
-                   "launch": getattr(args, "timing", "eager")},
+                   "launch": getattr(args, "timing", "eager"),
+                   "kernel_launch": "programmatic" if _env_flag("BOOST_PDL", 1) else "plain",
+                   "backward_streams": "forked" if _forked() else "one"},
         "tflops_per_s": tflops,
         "model_tflops_per_s": world * model * args.steps / (ms_total / 1e3) / 1e12,
         "pct_of_roofline": 100.0 * roof_ms / ms_step,

@@ -172,6 +172,19 @@ def test_report_line_carries_the_contract_keys(capsys):
     assert line["step_ms"]["median"] == pytest.approx(3.7)
 
 
+def test_launch_switches_read_like_the_library(monkeypatch):
+    # the library reads BOOST_PDL (default on) and BOOST_FORK_STREAMS (default off) with
+    # atoi: non-zero is on; bench.py reports the same reading in its config
+    monkeypatch.delenv("BOOST_PDL", raising=False)
+    monkeypatch.delenv("BOOST_FORK_STREAMS", raising=False)
+    assert bench._env_flag("BOOST_PDL", 1) and not bench._forked()
+    monkeypatch.setenv("BOOST_PDL", "0")
+    monkeypatch.setenv("BOOST_FORK_STREAMS", "1")
+    assert not bench._env_flag("BOOST_PDL", 1) and bench._forked()
+    monkeypatch.setenv("BOOST_PDL", "2")
+    assert bench._env_flag("BOOST_PDL", 1)
+
+
 def test_more_than_one_gpu_prints_unavailable_and_launches_nothing(capsys, monkeypatch):
     # the GEMMs use cluster-multicast TMA loads, which run in single-GPU processes only:
     # a request for 2 GPUs (flag or torchrun environment) prints one line and returns 0
