@@ -259,3 +259,49 @@ def test_header_compiles_as_plain_c_and_cpp(lang, std):
     r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, std, hdr],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def _kernel_bodies(path):
+    """name -> body text of every __global__ function in a CUDA source file."""
+    text = open(path).read()
+    out = {}
+    for m in re.finditer(r"__global__\s+void\s+(?:__launch_bounds__\([^)]*\)\s+)?(\w+)\s*\(",
+                         text):
+        start = text.index("{", text.index(")", m.end()))
+        depth, i = 0, start
+        while True:
+            depth += {"{": 1, "}": -1}.get(text[i], 0)
+            i += 1
+            if depth == 0:
+                break
+        out[m.group(1)] = text[start + 1:i - 1]
+    return out
+
+
+def test_programmatic_launches_wait_before_touching_memory():
+    # kernels launched with the programmatic-stream-serialisation attribute may start
+    # while the kernel before them runs: each must wait (griddepcontrol.wait) before any
+    # global memory access. The CUDA-core kernels launched through launch_k / launch_kb
+    # begin with pdl_enter(); the GEMM waits after its prologue (shared memory, TMEM and
+    # the parameter-space tensor maps only), before its roles start.
+    csrc = os.path.join(ROOT, "rank_bottleneck_online_gb300", "csrc")
+    simple = open(os.path.join(csrc, "kernels_simple.cu")).read()
+    launched = set(re.findall(r"launch_kb?\((\w+)", simple))
+    launched |= set(re.findall(r"\?\s*(\w+_kernel)\b", simple))
+    launched |= set(re.findall(r":\s*(\w+_kernel)\b", simple))
+    launched = {k.split("<")[0] for k in launched if k.endswith("_kernel")}
+    bodies = _kernel_bodies(os.path.join(csrc, "kernels_simple.cu"))
+    assert launched and launched <= set(bodies), launched - set(bodies)
+    for name in launched:
+        first = bodies[name].strip().split(";")[0].strip()
+        assert first == "pdl_enter()", f"{name} starts with {first!r}"
+    assert "<<<" not in simple.split("launch_wait_timeout_probe")[0], \
+        "plain launches before the probe: use launch_k"
+    gemm = _kernel_bodies(os.path.join(csrc, "gemm.cuh"))["gemm_kernel"]
+    wait = gemm.index("griddep_wait();")
+    assert gemm.index("griddep_launch_dependents();") > wait
+    assert wait < gemm.index("if (warp == 0) {\n    // ------") , \
+        "the GEMM must wait before its roles start"
+    for access in ("p.err", "p.out", "p.rstd", "p.qpart", "p.dgpart", "p.res"):
+        pos = gemm.find(access)
+        assert pos == -1 or pos > wait, f"{access} used before griddep_wait"
